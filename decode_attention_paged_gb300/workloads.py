@@ -1,0 +1,156 @@
+"""Seeded synthetic inputs for paged MLA decode.
+
+This module only draws random inputs: it holds none of the attention
+arithmetic, so both the CUDA path and the CPU oracle can be fed from it.
+
+Every tensor is made on the CPU with ``torch.Generator`` (seeds: q = 1,
+k_cache = 2, block_table = 3, seqlens = 4, plus an optional offset), values
+~N(0, 1) rounded to bf16, pages of 64 tokens, one KV head of 576 dims whose
+first 512 dims are also V.  The shapes are those of the decode workloads the
+FlashMLA pages discuss ("[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成
+GPU 吞吐", sec. 3 tensor shapes; FlashMLA deep dive, "如何在仓库中验证与复现":
+h_q = 128, h_kv = 1, d = 576, dv = 512, block size 64); the benchmark script
+they name is not available, so these synthetic workloads stand in for it.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional, Sequence
+
+import torch
+
+D_QK = 576
+D_V = 512
+PAGE = 64
+SCALE = D_QK ** -0.5
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    q: torch.Tensor            # [b, s_q, h_q, 576] bf16
+    k_cache: torch.Tensor      # [num_pages, 64, 1, 576] bf16
+    block_table: torch.Tensor  # [b, max_blocks] int32
+    cache_seqlens: torch.Tensor  # [b] int32
+    softmax_scale: float
+    causal: bool
+
+    @property
+    def b(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def s_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def h_q(self) -> int:
+        return self.q.shape[2]
+
+    def to(self, device) -> "Workload":
+        return dataclasses.replace(
+            self, q=self.q.to(device), k_cache=self.k_cache.to(device),
+            block_table=self.block_table.to(device), cache_seqlens=self.cache_seqlens.to(device))
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return g
+
+
+def _randn_bf16(shape, seed: int) -> torch.Tensor:
+    # Drawn in chunks of pages so that the peak fp32 footprint stays small.
+    out = torch.empty(shape, dtype=torch.bfloat16)
+    flat = out.view(-1)
+    g = _gen(seed)
+    step = 1 << 24
+    for s in range(0, flat.numel(), step):
+        e = min(flat.numel(), s + step)
+        flat[s:e] = torch.randn(e - s, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
+def make(name: str, b: int, s_q: int, h_q: int, seqlens: Sequence[int], num_pages: int,
+         max_blocks: Optional[int] = None, causal: bool = False, seed_offset: int = 0,
+         block_table: Optional[torch.Tensor] = None, scale: float = SCALE) -> Workload:
+    """Generic workload: block_table = randperm(num_pages)[:b*max_blocks].view(b, max_blocks)
+    unless given."""
+    seqlens = torch.tensor(list(seqlens), dtype=torch.int32)
+    assert seqlens.numel() == b
+    need = max(1, max((int(x) + PAGE - 1) // PAGE for x in seqlens.tolist()) if b else 1)
+    if max_blocks is None:
+        max_blocks = need
+    assert max_blocks >= need
+    if block_table is None:
+        assert num_pages >= b * max_blocks, "page pool too small for a permutation"
+        perm = torch.randperm(num_pages, generator=_gen(3 + seed_offset)).to(torch.int32)
+        block_table = perm[: b * max_blocks].view(b, max_blocks).contiguous()
+    q = _randn_bf16((b, s_q, h_q, D_QK), 1 + seed_offset)
+    k_cache = _randn_bf16((num_pages, PAGE, 1, D_QK), 2 + seed_offset)
+    return Workload(name, q, k_cache, block_table.to(torch.int32), seqlens, scale, causal)
+
+
+def tiny() -> Workload:
+    """batch 1, s_q 1, h_q 16, 4 pages, identity block table, L = 256, non-causal."""
+    bt = torch.arange(4, dtype=torch.int32).view(1, 4)
+    return make("tiny b1 s_q1 h_q16 L256", 1, 1, 16, [256], 4, 4, block_table=bt)
+
+
+def memory_bound() -> Workload:
+    """batch 64, s_q 1, h_q 16, every L = 4096, 4096 pages permuted."""
+    return make("memory-bound b64 s_q1 h_q16 L4096", 64, 1, 16, [4096] * 64, 4096, 64)
+
+
+def compute_bound() -> Workload:
+    """batch 64, s_q 1, h_q 128, L ~ U[1, 8192] (seed 4), 64*128 pages permuted."""
+    L = torch.randint(1, 8193, (64,), generator=_gen(4), dtype=torch.int64).tolist()
+    return make("compute-bound b64 s_q1 h_q128 L~U[1,8192]", 64, 1, 128, L, 64 * 128, 128)
+
+
+def mtp() -> Workload:
+    """batch 128, s_q 2, h_q 128, causal within the 2 query tokens, L = 4096."""
+    return make("MTP b128 s_q2 h_q128 causal L4096", 128, 2, 128, [4096] * 128, 8192, 64,
+                causal=True)
+
+
+def long_ragged() -> Workload:
+    """batch 8, s_q 1, h_q 64, L = 1 .. 65536, 8192 pages, 1024 blocks per row."""
+    L = [1, 64, 1000, 8191, 16384, 32768, 49152, 65536]
+    return make("long ragged b8 s_q1 h_q64 L<=65536", 8, 1, 64, L, 8192, 1024)
+
+
+CONFIGS = {
+    "tiny": tiny,
+    "memory_bound": memory_bound,
+    "compute_bound": compute_bound,
+    "mtp": mtp,
+    "long_ragged": long_ragged,
+}
+CONFIG_ORDER = ["tiny", "memory_bound", "compute_bound", "mtp", "long_ragged"]
+
+
+def random_case(seed: int, b: int, s_q: int, h_q: int, seqlens: Sequence[int], causal: bool,
+                extra_pages: int = 3) -> Workload:
+    """A small random case whose pool has a few pages no sequence references."""
+    need = max(1, max((int(x) + PAGE - 1) // PAGE for x in seqlens))
+    return make(f"random seed{seed}", b, s_q, h_q, seqlens, b * need + extra_pages, need,
+                causal=causal, seed_offset=10 * seed)
+
+
+def flops(seqlens: Sequence[int], s_q: int, h_q: int, causal: bool) -> int:
+    """Algorithmic FLOPs: 2*(576+512) per (query row, visible key)."""
+    total = 0
+    for L in seqlens:
+        L = int(L)
+        for s in range(s_q):
+            vis = max(0, min(L, L - s_q + s + 1)) if causal else L
+            total += vis * h_q
+    return total * 2 * (D_QK + D_V)
+
+
+def hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int) -> int:
+    """Algorithmic bytes: every cached token once (1152 B), q in, out and lse out."""
+    rows = len(seqlens) * s_q * h_q
+    return sum(int(L) for L in seqlens) * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)

@@ -1,0 +1,194 @@
+"""fp64 CPU oracle for paged MLA decode -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never imports, links or calls it, and shares no code with it.
+
+The C sources (``mla_oracle.c``, ``plan_oracle.c``) hold the arithmetic and
+cite the pages they follow; this module only compiles them with gcc and
+marshals numpy arrays through ctypes.
+
+Inputs are raw bf16 bit patterns (``uint16`` arrays); the C code widens them to
+fp64 exactly.  Outputs are fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "liboracle.so")
+_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "plan_oracle.c")]
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (plain C, fp64, no FMA
+    contraction so x86 and Arm give the same bits)."""
+    newest = max(os.path.getmtime(s) for s in _SRCS)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= newest:
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-pthread", "-o", tmp] + _SRCS + ["-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_SO)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            I64 = ctypes.c_int64
+            lib.oracle_mla_decode.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, D, I, P, P, I]
+            lib.oracle_mla_decode.restype = I
+            lib.oracle_mla_decode_rows.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, D, I, P,
+                                                   I64, P, P, I]
+            lib.oracle_mla_decode_rows.restype = I
+            lib.oracle_mla_partial.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, I, I,
+                                               I, P, P]
+            lib.oracle_mla_partial.restype = I
+            lib.oracle_merge_pair.argtypes = [P, P, P, D, D, P, I]
+            lib.oracle_merge_pair.restype = None
+            lib.oracle_lse_combine.argtypes = [I, P, P, I, P, P]
+            lib.oracle_lse_combine.restype = None
+            lib.oracle_plan.argtypes = [P, I, I, I, I, P, P]
+            lib.oracle_plan.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def bf16_bits(t) -> np.ndarray:
+    """uint16 bit patterns of a torch bf16 tensor (CPU), C-contiguous."""
+    import torch
+
+    assert t.dtype == torch.bfloat16
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy()).view(np.uint16)
+
+
+class Problem:
+    """One decode problem in the oracle's layout.
+
+    q      : uint16 [b, s_q, h_q, d]        (bf16 bits)
+    kv     : uint16 [num_pages, page, d]    (bf16 bits, the single KV head)
+    block_table : int32 [b, max_blocks]
+    seqlens     : int32 [b]
+    """
+
+    def __init__(self, q, kv, block_table, seqlens, scale, causal):
+        self.q = np.ascontiguousarray(q, dtype=np.uint16)
+        kv = np.asarray(kv, dtype=np.uint16)
+        if kv.ndim == 4:  # [pages, page, h_kv=1, d]
+            assert kv.shape[2] == 1
+            kv = kv.reshape(kv.shape[0], kv.shape[1], kv.shape[3])
+        self.kv = np.ascontiguousarray(kv)
+        self.block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        self.seqlens = np.ascontiguousarray(seqlens, dtype=np.int32)
+        self.b, self.s_q, self.h_q, self.d = self.q.shape
+        self.num_pages, self.page, d2 = self.kv.shape
+        assert d2 == self.d
+        self.max_blocks = self.block_table.shape[1] if self.block_table.ndim == 2 else 0
+        self.scale = float(scale)
+        self.causal = int(bool(causal))
+
+    def _args(self, dv):
+        return (_ptr(self.q), _ptr(self.kv), _ptr(self.block_table), _ptr(self.seqlens), self.b,
+                self.s_q, self.h_q, self.d, dv, self.page, self.max_blocks, self.num_pages,
+                self.scale, self.causal)
+
+
+def mla_decode(p: Problem, dv: int = 512, nthreads: int = 1):
+    """Full decode: returns (out [b, s_q, h_q, dv] fp64, lse [b, h_q, s_q] fp64)."""
+    lib = _load()
+    out = np.zeros((p.b, p.s_q, p.h_q, dv), dtype=np.float64)
+    lse = np.zeros((p.b, p.h_q, p.s_q), dtype=np.float64)
+    st = lib.oracle_mla_decode(*p._args(dv), _ptr(out), _ptr(lse), int(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_mla_decode failed: {st}")
+    return out, lse
+
+
+def mla_decode_rows(p: Problem, units, dv: int = 512, nthreads: int = 1):
+    """Selected rows only.  units: int array [n, 2] of (request, row = s*h_q + h).
+    Returns (out [n, dv], lse [n]) in fp64."""
+    lib = _load()
+    units = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+    n = units.shape[0]
+    out = np.zeros((n, dv), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    st = lib.oracle_mla_decode_rows(*p._args(dv), _ptr(units), n, _ptr(out), _ptr(lse),
+                                    int(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_mla_decode_rows failed: {st}")
+    return out, lse
+
+
+def mla_partial(p: Problem, i: int, rho: int, t_begin: int, t_end: int, dv: int = 512):
+    """Partial (normalised o[dv], lse) of row rho of request i over keys [t_begin, t_end)."""
+    lib = _load()
+    o = np.zeros((dv,), dtype=np.float64)
+    lse = np.zeros((1,), dtype=np.float64)
+    st = lib.oracle_mla_partial(*p._args(dv), int(i), int(rho), int(t_begin), int(t_end), _ptr(o),
+                                _ptr(lse))
+    if st != 0:
+        raise RuntimeError(f"oracle_mla_partial failed: {st}")
+    return o, float(lse[0])
+
+
+def merge_pair(state1, state2):
+    """Two-way merge of unnormalised states (m, l, o~).  Returns a new state."""
+    lib = _load()
+    m1, l1, o1 = state1
+    m2, l2, o2 = state2
+    m = np.array([m1], dtype=np.float64)
+    l = np.array([l1], dtype=np.float64)
+    o = np.array(o1, dtype=np.float64, copy=True)
+    o2 = np.ascontiguousarray(o2, dtype=np.float64)
+    lib.oracle_merge_pair(_ptr(m), _ptr(l), _ptr(o), float(m2), float(l2), _ptr(o2), o.shape[0])
+    return float(m[0]), float(l[0]), o
+
+
+def lse_combine(lse_parts, o_parts):
+    """n-way combine of normalised partials.  lse_parts [n], o_parts [n, dv]."""
+    lib = _load()
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64).reshape(-1)
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64).reshape(lse_parts.shape[0], -1)
+    dv = o_parts.shape[1]
+    o = np.zeros((dv,), dtype=np.float64)
+    lse = np.zeros((1,), dtype=np.float64)
+    lib.oracle_lse_combine(lse_parts.shape[0], _ptr(lse_parts), _ptr(o_parts), dv, _ptr(o),
+                           _ptr(lse))
+    return o, float(lse[0])
+
+
+PLAN_FIELDS = ("begin_req", "end_req", "begin_block", "end_block", "begin_split_idx",
+               "is_first_req_splitted", "is_last_req_splitted", "pad")
+
+
+def plan(seqlens, num_parts: int, fixed_overhead: int, page: int = 64):
+    """Tile-scheduler plan: returns (parts int32 [num_parts, 8], num_splits int32 [b+1])."""
+    lib = _load()
+    seqlens = np.ascontiguousarray(seqlens, dtype=np.int32).reshape(-1)
+    b = seqlens.shape[0]
+    parts = np.zeros((num_parts, 8), dtype=np.int32)
+    ns = np.zeros((b + 1,), dtype=np.int32)
+    st = lib.oracle_plan(_ptr(seqlens), b, int(page), int(num_parts), int(fixed_overhead),
+                         _ptr(parts), _ptr(ns))
+    if st != 0:
+        raise RuntimeError(f"oracle_plan failed: {st}")
+    return parts, ns
