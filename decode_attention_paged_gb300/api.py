@@ -1,0 +1,123 @@
+"""Python binding of libmla.so: argument marshalling only.
+
+Every step of the decode path (tile scheduling, paged TMA gathers, tcgen05
+QK^T / PV, online softmax, split combine) runs in the library's CUDA kernels.
+PyTorch only provides device memory (torch.empty) and the current stream.
+The functions carry the C ABI's names; see include/mla_decode.h for the exact
+contract of each.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+D_QK = 576
+D_V = 512
+PAGE = 64
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def metadata_size(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> Tuple[int, int]:
+    mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _lib.check(_lib.load().mla_metadata_size(batch, h_q, s_q, h_kv, ctypes.byref(mb),
+                                             ctypes.byref(sb)), "mla_metadata_size")
+    return mb.value, sb.value
+
+
+def workspace_size(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> int:
+    b = ctypes.c_size_t()
+    _lib.check(_lib.load().mla_workspace_size(batch, h_q, s_q, h_kv, ctypes.byref(b)),
+               "mla_workspace_size")
+    return b.value
+
+
+def mla_get_metadata(cache_seqlens: torch.Tensor, h_q: int, s_q: int, h_kv: int = 1,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Tile-scheduler plan for one decode step.  Returns (meta int32 [header + parts*8],
+    num_splits int32 [batch + 1]), both on cache_seqlens' device."""
+    assert cache_seqlens.is_cuda and cache_seqlens.dtype == torch.int32
+    cache_seqlens = cache_seqlens.contiguous()
+    batch = cache_seqlens.shape[0]
+    with torch.cuda.device(cache_seqlens.device):
+        mb, sb = metadata_size(batch, h_q, s_q, h_kv)
+        meta = torch.empty(mb // 4, dtype=torch.int32, device=cache_seqlens.device)
+        num_splits = torch.empty(sb // 4, dtype=torch.int32, device=cache_seqlens.device)
+        _lib.check(_lib.load().mla_get_metadata(_ptr(cache_seqlens), batch, h_q, s_q, h_kv,
+                                                _ptr(meta), _ptr(num_splits), _stream_ptr(stream)),
+                   "mla_get_metadata")
+    return meta, num_splits
+
+
+def mla_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
+                   cache_seqlens: torch.Tensor, softmax_scale: float, causal: bool,
+                   meta: torch.Tensor, num_splits: torch.Tensor,
+                   workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """out [b, s_q, h_q, 512] bf16 and lse [b, h_q, s_q] fp32 for absorbed queries
+    q [b, s_q, h_q, 576] over the paged cache k_cache [pages, 64, 1, 576]."""
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+    assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+    b, s_q, h_q, d = q.shape
+    assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and q.stride(1) == h_q * D_QK, \
+        "q rows must be packed: [b][s_q][h_q][576] with the (s_q, h_q) rows contiguous"
+    num_pages, page, h_kv, dk = k_cache.shape
+    assert dk == D_QK and k_cache.stride(3) == 1
+    assert block_table.stride(1) == 1
+    dev = q.device
+    with torch.cuda.device(dev):
+        if out is None:
+            out = torch.empty(b, s_q, h_q, D_V, dtype=torch.bfloat16, device=dev)
+        if lse is None:
+            lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
+        assert out.stride(3) == 1 and lse.is_contiguous()
+        if workspace is None:
+            workspace = torch.empty(workspace_size(b, h_q, s_q, h_kv), dtype=torch.uint8,
+                                    device=dev)
+        cache_seqlens = cache_seqlens.contiguous()
+        st = _lib.load().mla_decode_fwd(
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
+            page, _ptr(block_table), block_table.stride(0), block_table.shape[1],
+            _ptr(cache_seqlens), b, s_q, h_q, h_kv, float(softmax_scale), int(bool(causal)),
+            _ptr(meta), _ptr(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(out), out.stride(0), out.stride(1), out.stride(2), _ptr(lse), _stream_ptr(stream))
+        _lib.check(st, "mla_decode_fwd")
+    return out, lse
+
+
+def mla_last_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise the stream and read/clear the device error word."""
+    code = ctypes.c_int()
+    _lib.check(_lib.load().mla_last_device_error(_stream_ptr(stream), ctypes.byref(code)),
+               "mla_last_device_error")
+    return code.value
+
+
+def set_wait_budget_ns(ns: int) -> None:
+    _lib.check(_lib.load().mla_set_wait_budget_ns(int(ns)), "mla_set_wait_budget_ns")
+
+
+def set_fixed_overhead(blocks: int) -> None:
+    _lib.check(_lib.load().mla_set_fixed_overhead(int(blocks)), "mla_set_fixed_overhead")
+
+
+def flash_mla_with_kvcache(q, k_cache, block_table, cache_seqlens, head_dim_v, meta, num_splits,
+                           softmax_scale=None, causal=False):
+    """The pages' call shape (flash_mla_with_kvcache) mapped onto mla_decode_fwd."""
+    assert head_dim_v == D_V
+    if softmax_scale is None:
+        softmax_scale = q.shape[-1] ** -0.5
+    return mla_decode_fwd(q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                          num_splits)

@@ -1,0 +1,302 @@
+// mla_api.cu -- the C ABI of libmla.so (declared in include/mla_decode.h):
+// argument checking, the split-plan geometry, TMA descriptor encoding and the
+// kernel launches.  The library owns no device memory of its own apart from the
+// per-device error word below (a module global, not an allocation).
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+// First device-side error since the last mla_last_device_error() call.
+__device__ int g_mla_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
+constexpr int kDefaultFixedOverhead = 2;
+
+std::atomic<uint64_t> g_budget_ns{kDefaultBudgetNs};
+std::atomic<int> g_fixed_overhead{kDefaultFixedOverhead};
+
+struct DeviceInfo {
+    std::once_flag once;
+    int sms = 0;
+    int major = 0, minor = 0;
+    int* error_word = nullptr;
+    cudaError_t status = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return MLA_ERR_NO_DEVICE;
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo& d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        d.status = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.status == cudaSuccess)
+            d.status = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (d.status == cudaSuccess)
+            d.status = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (d.status == cudaSuccess)
+            d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), g_mla_error_word);
+    });
+    if (d.status != cudaSuccess) return MLA_ERR_CUDA;
+    // The kernels are built for sm_103a only.
+    if (d.major != 10 || d.minor != 3) return MLA_ERR_UNSUPPORTED;
+    *out = &d;
+    return MLA_OK;
+}
+
+int n_mtiles_of(int R) { return (R + kTileM - 1) / kTileM; }
+
+int num_parts_of(int R, int sms) {
+    const int mt = n_mtiles_of(R);
+    const int parts = sms / mt;
+    return parts > 0 ? parts : 1;
+}
+
+int check_shape(int batch, int h_q, int s_q, int h_kv) {
+    if (batch < 1 || h_q < 1 || s_q < 1 || batch > 65535) return MLA_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(s_q) * h_q > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace split: oaccum [pieces][R][512] fp32, then lseaccum [pieces][R].
+void workspace_layout(int batch, int R, int parts, size_t* o_bytes, size_t* total) {
+    const size_t pieces = static_cast<size_t>(batch) + parts;
+    *o_bytes = align_up(pieces * R * kDv * sizeof(float), 256);
+    *total = *o_bytes + align_up(pieces * R * sizeof(float), 256);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1) {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        g_encode_status = cudaGetDriverEntryPointByVersion(
+            "cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode), 12000,
+            cudaEnableDefault, &q);
+        if (g_encode_status == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_status = cudaErrorNotSupported;
+    });
+    if (g_encode_status != cudaSuccess || g_encode == nullptr) return MLA_ERR_CUDA;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {64, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARGUMENT;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_strerror(int code) {
+    switch (code) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MLA_ERR_CUDA: return "CUDA runtime error";
+        case MLA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+        case MLA_ERR_METADATA_MISMATCH: return "metadata was built for a different problem";
+        case MLA_ERR_NO_DEVICE: return "no CUDA device";
+        case MLA_ERR_SEQ_TOO_LONG: return "sequence longer than its block-table row";
+        case MLA_ERR_BAD_ALIGNMENT: return "pointer or stride breaks the 16-byte alignment rule";
+        default: return "unknown error";
+    }
+}
+
+int mla_version(void) { return 100; }
+
+int mla_set_wait_budget_ns(uint64_t budget_ns) {
+    g_budget_ns.store(budget_ns == 0 ? kDefaultBudgetNs : budget_ns);
+    return MLA_OK;
+}
+
+int mla_set_fixed_overhead(int blocks) {
+    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead : blocks);
+    return MLA_OK;
+}
+
+int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
+                      size_t* num_splits_bytes) {
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int parts = num_parts_of(s_q * h_q, d->sms);
+    if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
+    if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(batch) + 1);
+    return MLA_OK;
+}
+
+int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s_q, int h_kv,
+                     void* meta_dev, int32_t* num_splits_dev, mla_stream_t stream) {
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    if (!cache_seqlens_dev || !meta_dev || !num_splits_dev) return MLA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(meta_dev) & 3u) || (reinterpret_cast<uintptr_t>(num_splits_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cache_seqlens_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int R = s_q * h_q;
+    const int parts = num_parts_of(R, d->sms);
+    cudaError_t e = launch_sched(cache_seqlens_dev, batch, R, parts, n_mtiles_of(R),
+                                 g_fixed_overhead.load(), static_cast<int32_t*>(meta_dev),
+                                 num_splits_dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    if (!bytes) return MLA_ERR_INVALID_ARGUMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int R = s_q * h_q;
+    size_t ob = 0;
+    workspace_layout(batch, R, num_parts_of(R, d->sms), &ob, bytes);
+    return MLA_OK;
+}
+
+int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                   int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
+                   const int32_t* block_table_dev, int64_t bt_batch_stride, int max_blocks_per_seq,
+                   const int32_t* cache_seqlens_dev, int batch, int s_q, int h_q, int h_kv,
+                   float softmax_scale, int causal, const void* meta_dev,
+                   const int32_t* num_splits_dev, void* workspace_dev, size_t workspace_bytes,
+                   void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                   int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (!q_dev || !k_cache_dev || !block_table_dev || !cache_seqlens_dev || !meta_dev ||
+        !num_splits_dev || !out_dev || !lse_dev)
+        return MLA_ERR_INVALID_ARGUMENT;
+    if (num_pages < 1 || max_blocks_per_seq < 1 || bt_batch_stride < max_blocks_per_seq ||
+        q_batch_stride < static_cast<int64_t>(s_q) * h_q * kDqk || k_token_stride < kDqk ||
+        k_page_stride < k_token_stride * kPage || out_h_stride < kDv ||
+        out_s_stride < out_h_stride * h_q || out_batch_stride < out_s_stride * s_q ||
+        !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
+        return MLA_ERR_INVALID_ARGUMENT;
+    // TMA: 16-byte aligned bases and strides; vector stores: 16-byte aligned rows.
+    if (!aligned16(q_dev) || !aligned16(k_cache_dev) || !aligned16(out_dev) ||
+        (q_batch_stride % 8) || (k_page_stride % 8) || (k_token_stride % 8) ||
+        (out_batch_stride % 8) || (out_s_stride % 8) || (out_h_stride % 8) ||
+        (reinterpret_cast<uintptr_t>(lse_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int R = s_q * h_q;
+    const int parts = num_parts_of(R, d->sms);
+    size_t o_bytes = 0, ws_need = 0;
+    workspace_layout(batch, R, parts, &o_bytes, &ws_need);
+    if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
+
+    CUtensorMap q_map, kv_map;
+    const uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
+    st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
+                   kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
+    if (st) return st;
+    st = encode_3d(&kv_map, k_cache_dev, kDqk, kPage, static_cast<uint64_t>(num_pages),
+                   static_cast<uint64_t>(k_token_stride) * 2,
+                   static_cast<uint64_t>(k_page_stride) * 2, kPage);
+    if (st) return st;
+
+    DecodeParams p{};
+    p.block_table = block_table_dev;
+    p.bt_stride = bt_batch_stride;
+    p.max_blocks = max_blocks_per_seq;
+    p.seqlens = cache_seqlens_dev;
+    p.meta = static_cast<const int32_t*>(meta_dev);
+    p.num_splits = num_splits_dev;
+    p.out = static_cast<__nv_bfloat16*>(out_dev);
+    p.out_sb = out_batch_stride;
+    p.out_ss = out_s_stride;
+    p.out_sh = out_h_stride;
+    p.lse = lse_dev;
+    p.oaccum = static_cast<float*>(workspace_dev);
+    p.lseaccum = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + o_bytes);
+    p.batch = batch;
+    p.s_q = s_q;
+    p.h_q = h_q;
+    p.R = R;
+    p.n_mtiles = n_mtiles_of(R);
+    p.num_parts = parts;
+    p.q_box_rows = static_cast<int>(q_box_rows);
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.causal = causal;
+    p.error_word = d->error_word;
+    p.budget_ns = g_budget_ns.load();
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_decode(p, q_map, kv_map, s);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+
+    CombineParams c{};
+    c.meta = p.meta;
+    c.num_splits = num_splits_dev;
+    c.oaccum = p.oaccum;
+    c.lseaccum = p.lseaccum;
+    c.out = p.out;
+    c.out_sb = out_batch_stride;
+    c.out_ss = out_s_stride;
+    c.out_sh = out_h_stride;
+    c.lse = lse_dev;
+    c.batch = batch;
+    c.s_q = s_q;
+    c.h_q = h_q;
+    c.R = R;
+    e = launch_combine(c, s, /*pdl=*/true);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_last_device_error(mla_stream_t stream, int* code) {
+    if (!code) return MLA_ERR_INVALID_ARGUMENT;
+    DeviceInfo* d = nullptr;
+    int st = device_info(&d);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+    int v = 0, zero = 0;
+    if (cudaMemcpy(&v, d->error_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (cudaMemcpy(d->error_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    *code = v;
+    return MLA_OK;
+}
+
+}  // extern "C"

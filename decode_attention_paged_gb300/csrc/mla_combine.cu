@@ -1,0 +1,119 @@
+// mla_combine.cu -- merges the split-KV partial results of every request that
+// the tile scheduler cut into more than one piece.
+//
+// Source: "FlashMLA 新内核深度解析", section "Programmatic Dependent Launch": one
+// warp per query row takes the max of the pieces' log-sum-exps, weights each
+// partial output by exp2(lse_k - max), sums, and forms the final lse in the
+// log2 domain; the kernel waits for the decode grid with
+// cudaGridDependencySynchronize (griddepcontrol.wait) and reads the partials
+// with ordinary loads (not the read-only path, which does not see the
+// producer's writes under programmatic launch).  Pieces whose lse is -inf
+// (nothing visible) get weight 0; if every piece is empty the row is 0 and
+// lse -inf ("CUTLASS 从零重写 FlashAttention：Split KV 并行优化实战", sec. 3.3).
+//
+// Layout: oaccum [pieces][R][512] fp32 holds each piece's normalised output,
+// lseaccum [pieces][R] its log2-domain log-sum-exp (m + log2 l, with scores
+// already multiplied by softmax_scale * log2 e).  A warp owns one row: lane l
+// owns dims [16 l, 16 l + 16), so each piece is read as one contiguous 2 KB
+// burst per warp with 16-byte vector loads.
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+constexpr int kCombineWarps = 4;
+
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+    // Plain (coherent) global load; see the note on programmatic launch above.
+    float4 v;
+    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_f(const float* p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ int ld_i(const int32_t* p) {
+    int v;
+    asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombineParams p) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int req = blockIdx.y;
+    const int row = blockIdx.x * kCombineWarps + warp;
+    pdl_wait_primary();
+    if (row >= p.R) return;
+    // Metadata built for another shape: the decode kernel has already recorded
+    // MLA_ERR_METADATA_MISMATCH; num_splits may be too short to index.
+    if (ld_i(p.meta + kHMagic) != kMetaMagic || ld_i(p.meta + kHBatch) != p.batch ||
+        ld_i(p.meta + kHRows) != p.R)
+        return;
+    const int first = ld_i(p.num_splits + req);
+    const int n = ld_i(p.num_splits + req + 1) - first;
+    if (n <= 1) return;  // the decode kernel wrote this request directly
+
+    const float* lse_base = p.lseaccum + static_cast<int64_t>(first) * p.R + row;
+    float mx = -INFINITY;
+    for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ld_f(lse_base + static_cast<int64_t>(k) * p.R));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+
+    const int s = row / p.h_q, h = row % p.h_q;
+    __nv_bfloat16* orow = p.out + req * p.out_sb + s * p.out_ss + h * p.out_sh + lane * 16;
+    float* lse_out = p.lse + (static_cast<int64_t>(req) * p.h_q + h) * p.s_q + s;
+    if (mx == -INFINITY) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(orow)[0] = z;
+        reinterpret_cast<uint4*>(orow)[1] = z;
+        if (lane == 0) *lse_out = -INFINITY;
+        return;
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
+    for (int k = 0; k < n; ++k) {
+        const float lk = ld_f(lse_base + static_cast<int64_t>(k) * p.R);
+        const float w = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
+        if (w == 0.f) continue;  // never touch an empty piece's (unwritten) output
+        wsum += w;
+        const float* src = o_base + static_cast<int64_t>(k) * p.R * kDv;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            float4 x = ld_f4(src + 4 * v);
+            acc[4 * v + 0] += w * x.x;
+            acc[4 * v + 1] += w * x.y;
+            acc[4 * v + 2] += w * x.z;
+            acc[4 * v + 3] += w * x.w;
+        }
+    }
+    const float inv = 1.f / wsum;
+    uint32_t packed[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    reinterpret_cast<uint4*>(orow)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    reinterpret_cast<uint4*>(orow)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if (lane == 0) *lse_out = (mx + fast_log2(wsum)) * 0.69314718055994531f;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.R + kCombineWarps - 1) / kCombineWarps, p.batch, 1);
+    cfg.blockDim = dim3(32 * kCombineWarps, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+}
+
+}  // namespace mla

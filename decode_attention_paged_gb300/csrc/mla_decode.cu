@@ -1,0 +1,555 @@
+// mla_decode.cu -- persistent split-KV paged MLA decode kernel for sm_103a.
+//
+// Sources (web pages, cited by title and section):
+//   [Overview] "[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐":
+//       sec. 3 (one 576-dim cache row is K; its first 512 dims are V),
+//       sec. 4 (paged KV through block_table), sec. 6 (split-KV partials),
+//       sec. 7 (online softmax makes the partials mergeable).
+//   [DeepDive] "FlashMLA 新内核深度解析：Seesaw 调度、细粒度 TMA 流水线与 H800
+//       上的 660 TFlops MLA 解码": "细粒度 TMA copy-GEMM 流水线" (a 64x576 K
+//       tile moves as 9 TMA copies of 64x64), "缓存提示" (EVICT_FIRST on the
+//       streamed KV and on Q), exp -> exp2 with the scale folded in (the Seesaw
+//       section's closing note), "Programmatic Dependent Launch", "Tile
+//       Scheduler" (one CTA group per SM part walks its DecodingSchedMeta).
+//   [AttnBook] "3.4 Attention kernel": "在线 softmax" (m, l, o~ with the
+//       e^(m - m') rescale), 代码 (bottom-right causal mask).
+//
+// Design for sm_103a (what differs from the Hopper kernel on those pages):
+//   - One CTA per SM part and 64-query-row tile ("m-tile"); grid =
+//     (ceil(R / 64), num_sm_parts), at most one CTA per SM (227 KB smem).
+//   - The output tile O [64 x 512] fp32 lives in tensor memory, not registers:
+//     weight-stationary MMAs with M = 64 use the 2x2 datapath, so O takes 256
+//     of the 512 TMEM columns (lanes 0..63 hold dims [0,128) and [256,384),
+//     lanes 64..127 dims [128,256) and [384,512)).  This removes the register
+//     pressure that motivated the Seesaw schedule, so there is one output
+//     tile and no seesaw.
+//   - S = Q K^T [64 x 64] goes to TMEM too (32 columns per buffer, two
+//     buffers): lanes 0..63 hold tokens 0..31 of each row, lanes 64..127
+//     tokens 32..63, so a row's max is combined from two threads.
+//   - Warp roles: warp 0 = TMA producer (one thread), warp 1 = TMEM owner and
+//     MMA issuer (one thread), warps 2..5 = softmax / correction / epilogue
+//     (one thread per TMEM lane).
+//   - Q and each 64-token page are TMA-loaded as 9 chunks of [64 x 64] bf16
+//     with 128-byte swizzle; V is the first 8 chunks of the same page, read by
+//     the PV MMA as an MN-major operand, so the page is loaded once.
+//   - Lazy rescaling: the running max used for exponentiation only moves when
+//     a tile's max exceeds it by more than 8 (log2 units); otherwise O and l
+//     keep their scale.  Exact up to rounding: the final lse uses the max that
+//     was actually used.
+//   - Every wait is bounded (wall clock); on a timeout the CTA records
+//     MLA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+//     returns.  Waits in the softmax warps are taken by lane 0 and broadcast,
+//     so control flow stays warp-uniform.
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kQBytes = kChunks * kChunkBytes;      // 73728
+constexpr uint32_t kStageBytes = kChunks * kChunkBytes;  // 73728
+constexpr uint32_t kPBytes = 64 * 128;                   // P [64 rows x 64 tokens] bf16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;    // O: two PV halves of 128 columns
+constexpr uint32_t kColS = 256;  // S: two buffers of 32 columns
+constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
+// Draining waits for copies/MMAs this CTA issued itself; they finish on their
+// own, so the drain has its own budget, independent of the (possibly tiny)
+// wait budget a caller set.
+constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+
+struct Barriers {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t q_full, q_empty;
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full, pv_done, o_free, grp, drain;
+};
+
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kQBytes;
+constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
+constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kOffRedMax = kOffBar + 256;          // float [2][128]
+constexpr uint32_t kOffRedL = kOffRedMax + 2 * 128 * 4;  // float [2][128]
+constexpr uint32_t kOffMisc = kOffRedL + 2 * 128 * 4;    // tmem base, abort flag
+constexpr uint32_t kSmemBytes = kOffMisc + 64;
+static_assert(sizeof(Barriers) <= 256, "barrier block");
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+
+struct Part {
+    int begin_req, end_req, begin_block, end_block, begin_split;
+};
+
+__device__ __forceinline__ int blocks_of(int L) { return L > 0 ? (L + kPage - 1) / kPage : 0; }
+
+// Blocks [b0, b1) of request `req` that this part owns, clamped to the
+// sequence.  Every role calls this with the same inputs, so all roles see the
+// same list of work items.
+__device__ __forceinline__ void item_range(const DecodeParams& p, const Part& part, int req,
+                                           int& L, int& nb, int& b0, int& b1) {
+    L = p.seqlens[req];
+    if (L < 0) L = 0;
+    nb = blocks_of(L);
+    if (nb > p.max_blocks) nb = p.max_blocks;  // reported as MLA_ERR_SEQ_TOO_LONG
+    if (L > nb * kPage) L = nb * kPage;
+    b0 = (req == part.begin_req) ? part.begin_block : 0;
+    b1 = (req == part.end_req) ? part.end_block : nb;
+    if (b1 > nb) b1 = nb;
+    if (b0 < 0) b0 = 0;
+    if (b0 > b1) b0 = b1;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, wc, MLA_ERR_DEVICE_TIMEOUT);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+// One arrival per warp, after every lane's prior writes.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence_block();
+        mbar_arrive(bar);
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap q_map,
+                  const __grid_constant__ CUtensorMap kv_map) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int mtile = blockIdx.x, part_idx = blockIdx.y;
+
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sKV = smem + kOffKV;
+    uint8_t* sP = smem + kOffP;
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
+    float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
+    float* red_l = reinterpret_cast<float*>(smem + kOffRedL);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
+
+    // ------------------------------------------------------------ prologue
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_empty[s], 4);
+        }
+        mbar_init(&bars->p_full, 4);
+        mbar_init(&bars->pv_done, 1);
+        mbar_init(&bars->o_free, 4);
+        mbar_init(&bars->grp, 4);
+        mbar_init(&bars->drain, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&q_map);
+        prefetch_tensormap(&kv_map);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    // Query rows a partial Q tile load does not bring must read as zeros.
+    if (p.q_box_rows < kTileM) {
+        for (int i = tid; i < kChunks * kTileM * 8; i += kThreads) {
+            const int c = i / (kTileM * 8), rem = i % (kTileM * 8), r = rem / 8;
+            if (r >= p.q_box_rows)
+                reinterpret_cast<uint4*>(sQ + c * kChunkBytes)[rem] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // Everything above touched only on-chip state; global inputs may be
+    // written by the preceding kernel on the stream (programmatic launch).
+    pdl_wait_primary();
+
+    bool ok = (smem_u32(smem) & 1023u) == 0;
+    const int32_t* hdr = p.meta;
+    if (ok && (hdr[kHMagic] != kMetaMagic || hdr[kHBatch] != p.batch || hdr[kHRows] != p.R ||
+               hdr[kHParts] != p.num_parts || hdr[kHMTiles] != p.n_mtiles ||
+               hdr[kHPage] != kPage))
+        ok = false;
+    Part part{};
+    if (ok) {
+        const int32_t* rec = hdr + kMetaHeader + part_idx * kMetaFields;
+        part.begin_req = rec[kBeginReq];
+        part.end_req = rec[kEndReq];
+        part.begin_block = rec[kBeginBlock];
+        part.end_block = rec[kEndBlock];
+        part.begin_split = rec[kBeginSplit];
+        if (part.begin_req < p.batch &&
+            (part.begin_req < 0 || part.end_req >= p.batch || part.end_req < part.begin_req))
+            ok = false;
+        if (part.begin_req >= p.batch) part.end_req = part.begin_req - 1;  // empty part
+    }
+    if (!ok) {
+        if (tid == 0) raise_error(wc, MLA_ERR_METADATA_MISMATCH);
+        part.begin_req = 0;
+        part.end_req = -1;
+    }
+    if (tid == 0) {
+        for (int req = part.begin_req; req <= part.end_req; ++req) {
+            const int L = p.seqlens[req];
+            if (L > 0 && blocks_of(L) > p.max_blocks) raise_error(wc, MLA_ERR_SEQ_TOO_LONG);
+        }
+    }
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        const uint64_t policy = policy_evict_first();
+        uint32_t g = 0, n_items = 0;
+        const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
+        for (int req = part.begin_req; req <= part.end_req; ++req) {
+            int L, nb, b0, b1;
+            item_range(p, part, req, L, nb, b0, b1);
+            if (b1 <= b0) continue;
+            if (n_items > 0 && !mbar_wait(&bars->q_empty, (n_items - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
+                break;
+            mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+            for (int c = 0; c < kChunks; ++c)
+                tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c, mtile * kTileM,
+                            req, policy);
+            ++n_items;
+            bool stop = false;
+            for (int blk = b0; blk < b1; ++blk, ++g) {
+                const int st = g & 1;
+                if (g >= 2 && !mbar_wait(&bars->kv_empty[st], ((g >> 1) + 1) & 1, wc,
+                                         MLA_ERR_DEVICE_TIMEOUT)) {
+                    stop = true;
+                    break;
+                }
+                const int page = p.block_table[static_cast<int64_t>(req) * p.bt_stride + blk];
+                mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                uint8_t* dst = sKV + st * kStageBytes;
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
+                                policy);
+            }
+            if (stop) break;
+        }
+        // Drain: never leave the CTA with copies still landing in its smem.
+        for (uint32_t k = (g >= 2 ? g - 2 : 0); k < g; ++k)
+            mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
+        if (n_items > 0) mbar_drain(&bars->q_full, (n_items - 1) & 1, kDrainBudgetNs);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
+        const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV), sP_a = smem_u32(sP);
+        uint32_t g = 0, n_items = 0;
+        bool pend = false, pend_first = false;
+        uint32_t pend_g = 0, pend_item = 0;
+        bool alive = true;
+        auto issue_pv = [&](uint32_t pg, bool first_of_item, uint32_t item) -> bool {
+            if (!mbar_wait(&bars->p_full, pg & 1, wc, MLA_ERR_DEVICE_TIMEOUT)) return false;
+            if (first_of_item && item > 0 &&
+                !mbar_wait(&bars->o_free, (item - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
+                return false;
+            tc_fence_after();
+            const uint32_t v_base = sKV_a + (pg & 1) * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = smem_desc(sP_a + kk * 32, 16, 1024);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint64_t b = smem_desc(v_base + h * 4 * kChunkBytes + kk * 2048,
+                                                 kChunkBytes, 1024);
+                    mma_ws_ss(tmem + kColO + 128 * h, a, b, idesc_pv,
+                              (first_of_item && kk == 0) ? 0u : 1u);
+                }
+            }
+            mma_commit(&bars->pv_done);
+            mma_commit(&bars->kv_empty[pg & 1]);
+            return true;
+        };
+        for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
+            int L, nb, b0, b1;
+            item_range(p, part, req, L, nb, b0, b1);
+            if (b1 <= b0) continue;
+            if (!mbar_wait(&bars->q_full, n_items & 1, wc, MLA_ERR_DEVICE_TIMEOUT)) {
+                alive = false;
+                break;
+            }
+            for (int blk = b0; blk < b1; ++blk, ++g) {
+                const int st = g & 1;
+                if (!mbar_wait(&bars->kv_full[st], (g >> 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT) ||
+                    (g >= 2 && !mbar_wait(&bars->s_empty[st], ((g >> 1) + 1) & 1, wc,
+                                          MLA_ERR_DEVICE_TIMEOUT))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t k_base = sKV_a + st * kStageBytes;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = smem_desc(sQ_a + c * kChunkBytes + kk * 32, 16, 1024);
+                        const uint64_t b = smem_desc(k_base + c * kChunkBytes + kk * 32, 16, 1024);
+                        mma_ws_ss(tmem + kColS + 32 * st, a, b, idesc_qk, (c | kk) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&bars->s_full[st]);
+                if (blk == b1 - 1) mma_commit(&bars->q_empty);
+                if (pend && !issue_pv(pend_g, pend_first, pend_item)) {
+                    alive = false;
+                    pend = false;
+                    break;
+                }
+                pend = true;
+                pend_g = g;
+                pend_first = (blk == b0);
+                pend_item = n_items;
+            }
+            ++n_items;
+        }
+        if (alive && pend) issue_pv(pend_g, pend_first, pend_item);
+        // Drain: all MMAs finished before TMEM is released.
+        mma_commit(&bars->drain);
+        mbar_drain(&bars->drain, 0, kDrainBudgetNs);
+    } else if (warp >= 2) {
+        // ------------------------------------- softmax / correction / epilogue
+        const int q4 = warp & 3;
+        const int Lrow = 32 * q4 + lane;  // TMEM lane
+        const int r = Lrow & 63, half = Lrow >> 6;
+        const int row = mtile * kTileM + r;
+        const bool row_valid = row < p.R;
+        const int s_idx = row / p.h_q, h_idx = row % p.h_q;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        uint32_t gblk = 0, n_items = 0, grp_phase = 0;
+        bool alive = true;
+        auto group_sync = [&]() -> bool {
+            warp_arrive(&bars->grp);
+            const bool okw = warp_wait(&bars->grp, grp_phase & 1, wc);
+            ++grp_phase;
+            return okw;
+        };
+        for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
+            int L, nb, b0, b1;
+            item_range(p, part, req, L, nb, b0, b1);
+            int lim = L;
+            if (p.causal) {
+                lim = L - p.s_q + s_idx + 1;
+                lim = lim < 0 ? 0 : (lim > L ? L : lim);
+            }
+            const int first_piece = p.num_splits[req];
+            const bool split = (p.num_splits[req + 1] - first_piece) > 1;
+            const int slot = (req == part.begin_req) ? part.begin_split : first_piece;
+            float m_used = -INFINITY, l_part = 0.f;
+            for (int blk = b0; blk < b1; ++blk, ++gblk) {
+                const int st = gblk & 1;
+                if (!warp_wait(&bars->s_full[st], (gblk >> 1) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sv[32];
+                tmem_ld32(tl + kColS + 32 * st, sv);
+                tmem_ld_wait();
+                tc_fence_before();
+                warp_arrive(&bars->s_empty[st]);
+
+                const int t0 = blk * kPage + 32 * half;
+                float x[32];
+                float hmax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = (t0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+                    hmax = fmaxf(hmax, x[c]);
+                }
+                red_max[(gblk & 1) * 128 + Lrow] = hmax;
+                if (!group_sync()) {
+                    alive = false;
+                    break;
+                }
+                const float tmax = fmaxf(hmax, red_max[(gblk & 1) * 128 + (Lrow ^ 64)]);
+                float alpha = 1.f;
+                bool need = false;
+                if (tmax > m_used + kLazyThreshold) {
+                    alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tmax);
+                    m_used = tmax;
+                    need = true;
+                }
+                if (need) l_part *= alpha;
+                uint32_t pk[16];
+                float psum = 0.f;
+                const bool none = (m_used == -INFINITY);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = none ? 0.f : fast_exp2(x[2 * c] - m_used);
+                    const float p1 = none ? 0.f : fast_exp2(x[2 * c + 1] - m_used);
+                    psum += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                l_part += psum;
+
+                // The P buffer and O are free once the previous PV finished.
+                if (gblk > 0 && !warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need && blk > b0)) {
+                    const float a = (need && blk > b0) ? alpha : 1.f;
+#pragma unroll 1
+                    for (int cg = 0; cg < 8; ++cg) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + kColO + 32 * cg, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                        tmem_st32(tl + kColO + 32 * cg, o);
+                    }
+                    tmem_st_wait();
+                }
+                // Last page of the sequence: zero the V rows past its length so
+                // stale slots (even NaN) cannot reach P.V through 0 * x.
+                if (blk == nb - 1 && (L & (kPage - 1)) != 0) {
+                    const int tail0 = L & (kPage - 1);
+                    const int per_chunk = (kPage - tail0) * 8;  // 16-byte units
+                    uint8_t* stage = sKV + st * kStageBytes;
+                    for (int i = tid - 64; i < 8 * per_chunk; i += 128) {
+                        const int c = i / per_chunk, u = i % per_chunk;
+                        reinterpret_cast<uint4*>(stage + c * kChunkBytes + tail0 * 128)[u] =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = sw128_offset(r, 4 * half + k);
+                    *reinterpret_cast<uint4*>(sP + off) =
+                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                warp_arrive(&bars->p_full);
+            }
+            if (!alive) break;
+
+            // ---------------------------------------------------- epilogue
+            const bool has_blocks = b1 > b0;
+            float l_tot = 0.f;
+            if (has_blocks) {
+                if (!warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                red_l[(n_items & 1) * 128 + Lrow] = l_part;
+                if (!group_sync()) {
+                    alive = false;
+                    break;
+                }
+                l_tot = l_part + red_l[(n_items & 1) * 128 + (Lrow ^ 64)];
+            }
+            const bool empty = !(l_tot > 0.f);
+            const float inv = empty ? 0.f : 1.f / l_tot;
+            const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
+            const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
+            if (has_blocks) {
+#pragma unroll 1
+                for (int cg = 0; cg < 8; ++cg) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + kColO + 32 * cg, o);
+                    tmem_ld_wait();
+                    const int dv0 = 256 * (cg >> 2) + 128 * half + 32 * (cg & 3);
+                    if (!row_valid) continue;
+                    if (split) {
+                        float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv,
+                                                 __uint_as_float(o[4 * v + 1]) * inv,
+                                                 __uint_as_float(o[4 * v + 2]) * inv,
+                                                 __uint_as_float(o[4 * v + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            p.out + req * p.out_sb + s_idx * p.out_ss + h_idx * p.out_sh + dv0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                w[j] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * j]) * inv,
+                                                   __uint_as_float(o[8 * v + 2 * j + 1]) * inv);
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                warp_arrive(&bars->o_free);
+                ++n_items;
+            } else if (row_valid) {
+                if (split) {
+                    float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv);
+                    for (int v = 0; v < 64; ++v) dst[v * 2 + half] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + req * p.out_sb + s_idx * p.out_ss +
+                                                          h_idx * p.out_sh);
+                    for (int v = 0; v < 32; ++v) dst[v * 2 + half] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            if (row_valid && half == 0) {
+                if (split)
+                    p.lseaccum[acc_row] = lse2;
+                else
+                    p.lse[(static_cast<int64_t>(req) * p.h_q + h_idx) * p.s_q + s_idx] =
+                        empty ? -INFINITY : lse2 * 0.69314718055994531f;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
+                          const CUtensorMap& kv_map, cudaStream_t stream) {
+    static int configured_mask = 0;  // per-device "smem attribute set" bits (first 31 devices)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 31 || !(configured_mask & (1 << dev))) {
+        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_mtiles, p.num_parts, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel, p, q_map, kv_map);
+}
+
+}  // namespace mla

@@ -1,0 +1,191 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) paged MLA decode library
+ * (libmla.so).
+ *
+ * What it computes.  Multi-head Latent Attention decode after weight
+ * absorption: h_q query heads of dimension 576 attend to ONE shared paged KV
+ * head whose 576-dim rows (512 latent + 64 RoPE) serve as K, and whose first
+ * 512 dims serve as V ("[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU
+ * 吞吐", sec. 2 "Weight Absorption" and sec. 3 "一个 576 维缓存为什么同时充当 K
+ * 和 V").  For request i, query token s, head h:
+ *     visible  = { t < L_i : !causal || t <= L_i - s_q + s }
+ *     kv_t     = k_cache[block_table[i][t / 64]][t % 64][0][:]
+ *     x_t      = softmax_scale * dot(q[i][s][h][:], kv_t[0:576])
+ *     lse[i][h][s] = ln sum_t exp(x_t)                    (natural log)
+ *     out[i][s][h][:] = sum_t exp(x_t - lse) * kv_t[0:512]
+ * An empty visible set gives out = 0 and lse = -inf.  The causal rule is the
+ * bottom-right aligned triangle ("3.4 Attention kernel", 代码).
+ *
+ * The two calls follow the API of "FlashMLA 新内核深度解析" (section "如何在
+ * 仓库中验证与复现"): get_mla_metadata(cache_seqlens, s_q*h_q//h_kv, h_kv, ...)
+ * -> (tile_scheduler_metadata, num_splits), then flash_mla_with_kvcache(q,
+ * kvcache, block_table, cache_seqlens, dv, metadata, num_splits, causal) ->
+ * (out, lse).  Here they are mla_get_metadata and mla_decode_fwd.
+ *
+ * Conventions for every function:
+ *   - returns MLA_OK (0) or a negative MLA_ERR_* code; mla_strerror() names it;
+ *   - every pointer argument named *_dev is DEVICE memory, owned by the
+ *     caller; the library never allocates, frees or retains memory;
+ *   - work is enqueued asynchronously on `stream` (a cudaStream_t, 0 = the
+ *     legacy default stream) on the CURRENT device; no call synchronises the
+ *     stream except mla_last_device_error;
+ *   - argument errors are detected on the host before anything is enqueued
+ *     and leave every buffer untouched;
+ *   - errors that only the device can see (a sequence longer than its
+ *     block-table row, metadata built for another shape, a pipeline wait that
+ *     exceeded its time budget) are recorded in a per-device error word and
+ *     reported by mla_last_device_error().
+ * Supported: bf16 q / k_cache / out, fp32 lse, h_kv = 1, d_qk = 576,
+ * d_v = 512, page size 64, GPUs of compute capability 10.3 (GB300).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mla_stream_t; /* same type as cudaStream_t */
+
+/* Every entry point below is exported from libmla.so (built with hidden
+ * default visibility, so nothing else is). */
+#ifndef MLA_API
+#define MLA_API __attribute__((visibility("default")))
+#endif
+
+enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARGUMENT = -1,   /* null pointer, bad size or stride       */
+    MLA_ERR_UNSUPPORTED = -2,        /* h_kv != 1, page size != 64, wrong GPU   */
+    MLA_ERR_WORKSPACE_TOO_SMALL = -3,
+    MLA_ERR_CUDA = -4,               /* a CUDA runtime call failed              */
+    MLA_ERR_DEVICE_TIMEOUT = -5,     /* device: a pipeline wait ran out         */
+    MLA_ERR_METADATA_MISMATCH = -6,  /* device: metadata built for other shapes */
+    MLA_ERR_NO_DEVICE = -7,          /* no CUDA device visible                  */
+    MLA_ERR_SEQ_TOO_LONG = -8,       /* device: L_i > 64 * max_blocks_per_seq   */
+    MLA_ERR_BAD_ALIGNMENT = -9       /* a pointer/stride breaks 16-byte rules   */
+};
+
+#define MLA_HEAD_DIM_QK 576
+#define MLA_HEAD_DIM_V 512
+#define MLA_PAGE_SIZE 64
+
+/* Human-readable name of a status code (static string, never NULL). */
+MLA_API const char *mla_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+MLA_API int mla_version(void);
+
+/*
+ * mla_metadata_size -- bytes of the two metadata buffers for a problem shape.
+ * Source: "FlashMLA 新内核深度解析", section "Tile Scheduler" (DecodingSchedMeta
+ * per SM part, num_splits per request).
+ *   meta_bytes: int32 header[8] + num_sm_parts records of 8 int32 each, where
+ *     num_sm_parts = max(1, SMs / ceil(s_q*h_q / 64)) on the current device;
+ *   num_splits_bytes: int32[batch + 1].
+ * Either output pointer may be NULL.  Errors: INVALID_ARGUMENT for
+ * batch < 1, h_q < 1, s_q < 1; UNSUPPORTED for h_kv != 1; NO_DEVICE / CUDA
+ * when the device cannot be queried.
+ */
+MLA_API int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t *meta_bytes,
+                      size_t *num_splits_bytes);
+
+/*
+ * mla_get_metadata -- build the tile-scheduler plan on the device.
+ * Source: "FlashMLA 新内核深度解析", section "Tile Scheduler" (one warp counts
+ * every request's 64-token blocks, caps each SM part at
+ * payload = ceil(total / num_sm_parts) + fixed overhead, and walks the requests
+ * greedily, splitting a request over parts when it does not fit).
+ *   cache_seqlens_dev : int32[batch], device.  Negative values count as 0.
+ *   meta_dev          : device buffer of mla_metadata_size() meta_bytes,
+ *                       4-byte aligned; receives header + part records.
+ *   num_splits_dev    : device int32[batch + 1]; receives the prefix sum of the
+ *                       number of pieces each request is cut into.
+ * The plan is valid for mla_decode_fwd calls with the same batch, s_q, h_q,
+ * h_kv, cache_seqlens and device; it may be reused across layers of one step
+ * ("[DeepSeek-3] FlashMLA", sec. 5).  Enqueues one kernel on `stream`.
+ */
+MLA_API int mla_get_metadata(const int32_t *cache_seqlens_dev, int batch, int h_q, int s_q, int h_kv,
+                     void *meta_dev, int32_t *num_splits_dev, mla_stream_t stream);
+
+/*
+ * mla_workspace_size -- bytes of split-KV scratch mla_decode_fwd needs:
+ * fp32 partial outputs [pieces][s_q*h_q][512] and partial log-sum-exps
+ * [pieces][s_q*h_q], with pieces <= batch + num_sm_parts (every part boundary
+ * adds at most one piece).  Source: "[DeepSeek-3] FlashMLA", sec. 6
+ * (out_accum / lse_accum), "CUTLASS 从零重写 FlashAttention：Split KV 并行优化
+ * 实战" sec. 3.1 (caller-preallocated, aligned workspace).
+ */
+MLA_API int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t *bytes);
+
+/*
+ * mla_decode_fwd -- paged MLA decode: out, lse from q and the paged cache.
+ * Sources: "[DeepSeek-3] FlashMLA", sec. 3-7 (definition, paging, split-KV,
+ * online softmax); "FlashMLA 新内核深度解析", sections "细粒度 TMA copy-GEMM 流水
+ * 线", "缓存提示", "Programmatic Dependent Launch", "Tile Scheduler".
+ *
+ *   q_dev        bf16 [batch][s_q][h_q][576]; the 576 dims and the (s_q, h_q)
+ *                rows are packed (row stride 576, s stride h_q*576 elements);
+ *                q_batch_stride (elements) is free but a multiple of 8.
+ *                16-byte aligned.
+ *   k_cache_dev  bf16 [num_pages][64][h_kv = 1][576]; k_page_stride and
+ *                k_token_stride in elements, multiples of 8, the 576 dims
+ *                contiguous.  16-byte aligned.  Slots of the last page of a
+ *                sequence beyond its length never influence the result.
+ *   block_table_dev int32 [batch][max_blocks_per_seq], row stride
+ *                bt_batch_stride (elements).  Entries for blocks
+ *                < ceil(L_i / 64) must name pages in [0, num_pages); an entry
+ *                outside reads zeros (never out-of-bounds memory).
+ *   cache_seqlens_dev int32 [batch].
+ *   softmax_scale  multiplies q.k (the examples use 576^-0.5).
+ *   causal         0 or 1 (bottom-right aligned mask over the s_q tokens).
+ *   meta_dev, num_splits_dev  from mla_get_metadata for the same shapes.
+ *   workspace_dev  >= mla_workspace_size() bytes, 256-byte aligned.
+ *   out_dev      bf16 [batch][s_q][h_q][512]; element strides out_batch_stride,
+ *                out_s_stride, out_h_stride; dims contiguous; 16-byte aligned
+ *                rows.
+ *   lse_dev      fp32 [batch][h_q][s_q], contiguous.
+ * Enqueues the decode kernel and (programmatically dependent) the combine
+ * kernel on `stream`.  Graph-capturable: no allocation, no synchronisation.
+ */
+MLA_API int mla_decode_fwd(const void *q_dev, int64_t q_batch_stride, const void *k_cache_dev,
+                   int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
+                   const int32_t *block_table_dev, int64_t bt_batch_stride,
+                   int max_blocks_per_seq, const int32_t *cache_seqlens_dev, int batch, int s_q,
+                   int h_q, int h_kv, float softmax_scale, int causal, const void *meta_dev,
+                   const int32_t *num_splits_dev, void *workspace_dev, size_t workspace_bytes,
+                   void *out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                   int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
+
+/*
+ * mla_last_device_error -- synchronise `stream`, then read and clear the
+ * current device's error word.  *code receives MLA_OK or the first device-side
+ * MLA_ERR_* recorded since the last call.  Returns MLA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+MLA_API int mla_last_device_error(mla_stream_t stream, int *code);
+
+/*
+ * mla_set_wait_budget_ns -- wall-clock budget of every pipeline wait inside
+ * the decode kernel (default 2e9 ns).  When a wait runs out the kernel records
+ * MLA_ERR_DEVICE_TIMEOUT, drains its own copies and returns.  Tests use a tiny
+ * budget to exercise that path; 0 restores the default.  Process-wide.
+ */
+MLA_API int mla_set_wait_budget_ns(uint64_t budget_ns);
+
+/*
+ * mla_set_fixed_overhead -- the scheduler's fixed per-piece overhead in
+ * 64-token blocks (fixed_overhead_num_blocks in the "Tile Scheduler" section;
+ * default 2).  Affects only load balance, never results.  Process-wide;
+ * negative restores the default.
+ */
+MLA_API int mla_set_fixed_overhead(int blocks);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,60 @@
+"""The device tile scheduler (mla_get_metadata) against the oracle's plan:
+integer for integer, plus the plan invariants."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.test_plan_oracle import check_plan_invariants
+
+pytestmark = pytest.mark.gpu
+
+HEADER = 8
+
+
+def device_plan(seqlens, h_q, s_q):
+    from decode_attention_paged_gb300 import api
+
+    sl = torch.tensor(seqlens, dtype=torch.int32, device="cuda")
+    meta, ns = api.mla_get_metadata(sl, h_q, s_q)
+    torch.cuda.synchronize()
+    meta = meta.cpu().numpy()
+    return meta[:HEADER], meta[HEADER:].reshape(-1, 8), ns.cpu().numpy()
+
+
+CASES = [
+    ([256], 16, 1),
+    ([4096] * 64, 16, 1),
+    ([1, 64, 1000, 8191, 16384, 32768, 49152, 65536], 64, 1),
+    ([4096] * 128, 128, 2),
+    ([0, 0, 5, 0], 16, 1),
+    (list(range(0, 3000, 37)), 20, 3),
+    ([70000] * 3, 1, 1),
+]
+
+
+@pytest.mark.parametrize("seqlens,h_q,s_q", CASES)
+def test_device_plan_equals_oracle(seqlens, h_q, s_q):
+    hdr, parts, ns = device_plan(seqlens, h_q, s_q)
+    R = s_q * h_q
+    assert hdr[0] == 0x4D4C4131 and hdr[1] == len(seqlens) and hdr[2] == R
+    num_parts, n_mtiles, fixed = int(hdr[3]), int(hdr[4]), int(hdr[5])
+    assert n_mtiles == -(-R // 64)
+    assert num_parts == max(1, torch.cuda.get_device_properties(0).multi_processor_count // n_mtiles)
+    ref_parts, ref_ns = oracle.plan(seqlens, num_parts, fixed)
+    assert np.array_equal(parts, ref_parts)
+    assert np.array_equal(ns, ref_ns)
+    assert hdr[7] == ns[-1]
+    check_plan_invariants(seqlens, parts, ns, num_parts, fixed)
+
+
+def test_random_seqlens_plans():
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        b = int(rng.integers(1, 300))
+        seqlens = rng.integers(0, 20000, size=b).tolist()
+        h_q = int(rng.choice([1, 16, 64, 128]))
+        s_q = int(rng.choice([1, 2]))
+        hdr, parts, ns = device_plan(seqlens, h_q, s_q)
+        ref_parts, ref_ns = oracle.plan(seqlens, int(hdr[3]), int(hdr[5]))
+        assert np.array_equal(parts, ref_parts) and np.array_equal(ns, ref_ns)
