@@ -44,20 +44,86 @@ def workspace_size(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> int:
 
 
 def mla_get_metadata(cache_seqlens: torch.Tensor, h_q: int, s_q: int, h_kv: int = 1,
-                     stream: Optional[torch.cuda.Stream] = None):
+                     stream: Optional[torch.cuda.Stream] = None,
+                     meta: Optional[torch.Tensor] = None,
+                     num_splits: Optional[torch.Tensor] = None):
     """Tile-scheduler plan for one decode step.  Returns (meta int32 [header + parts*8],
-    num_splits int32 [batch + 1]), both on cache_seqlens' device."""
+    num_splits int32 [batch + 1]), both on cache_seqlens' device; pass meta /
+    num_splits to fill existing buffers (e.g. inside a CUDA graph)."""
     assert cache_seqlens.is_cuda and cache_seqlens.dtype == torch.int32
     cache_seqlens = cache_seqlens.contiguous()
     batch = cache_seqlens.shape[0]
     with torch.cuda.device(cache_seqlens.device):
         mb, sb = metadata_size(batch, h_q, s_q, h_kv)
-        meta = torch.empty(mb // 4, dtype=torch.int32, device=cache_seqlens.device)
-        num_splits = torch.empty(sb // 4, dtype=torch.int32, device=cache_seqlens.device)
+        if meta is None:
+            meta = torch.empty(mb // 4, dtype=torch.int32, device=cache_seqlens.device)
+        if num_splits is None:
+            num_splits = torch.empty(sb // 4, dtype=torch.int32, device=cache_seqlens.device)
+        assert meta.dtype == torch.int32 and meta.numel() * 4 >= mb and meta.is_contiguous()
+        assert num_splits.dtype == torch.int32 and num_splits.numel() * 4 >= sb
         _lib.check(_lib.load().mla_get_metadata(_ptr(cache_seqlens), batch, h_q, s_q, h_kv,
                                                 _ptr(meta), _ptr(num_splits), _stream_ptr(stream)),
                    "mla_get_metadata")
     return meta, num_splits
+
+
+class DecodeCall:
+    """Marshalled arguments of one decode call (validated shapes, allocated
+    outputs and workspace), reusable for the fused call or its two halves."""
+
+    def __init__(self, q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                 num_splits, workspace=None, out=None, lse=None, stream=None):
+        assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+        assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+        b, s_q, h_q, d = q.shape
+        assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
+            q.stride(1) == h_q * D_QK, \
+            "q rows must be packed: [b][s_q][h_q][576] with the (s_q, h_q) rows contiguous"
+        num_pages, page, h_kv, dk = k_cache.shape
+        assert dk == D_QK and k_cache.stride(3) == 1
+        assert block_table.stride(1) == 1
+        dev = q.device
+        with torch.cuda.device(dev):
+            if out is None:
+                out = torch.empty(b, s_q, h_q, D_V, dtype=torch.bfloat16, device=dev)
+            if lse is None:
+                lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
+            assert out.stride(3) == 1 and lse.is_contiguous()
+            if workspace is None:
+                workspace = torch.empty(workspace_size(b, h_q, s_q, h_kv), dtype=torch.uint8,
+                                        device=dev)
+        cache_seqlens = cache_seqlens.contiguous()
+        self.device = dev
+        self.out, self.lse, self.workspace = out, lse, workspace
+        self._keep = (q, k_cache, block_table, cache_seqlens, meta, num_splits)
+        self.stream = stream
+        ws_bytes = workspace.numel() * workspace.element_size()
+        self.full_args = (
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
+            page, _ptr(block_table), block_table.stride(0), block_table.shape[1],
+            _ptr(cache_seqlens), b, s_q, h_q, h_kv, float(softmax_scale), int(bool(causal)),
+            _ptr(meta), _ptr(num_splits), _ptr(workspace), ws_bytes, _ptr(out), out.stride(0),
+            out.stride(1), out.stride(2), _ptr(lse))
+        self.combine_args = (_ptr(meta), _ptr(num_splits), _ptr(workspace), ws_bytes, b, s_q, h_q,
+                             h_kv, _ptr(out), out.stride(0), out.stride(1), out.stride(2),
+                             _ptr(lse))
+
+    def fwd(self):
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.load().mla_decode_fwd(*self.full_args, _stream_ptr(self.stream)),
+                       "mla_decode_fwd")
+        return self.out, self.lse
+
+    def splitkv(self):
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.load().mla_decode_splitkv(*self.full_args, _stream_ptr(self.stream)),
+                       "mla_decode_splitkv")
+
+    def combine(self):
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.load().mla_decode_combine(*self.combine_args, _stream_ptr(self.stream)),
+                       "mla_decode_combine")
+        return self.out, self.lse
 
 
 def mla_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
@@ -68,33 +134,8 @@ def mla_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Te
                    stream: Optional[torch.cuda.Stream] = None):
     """out [b, s_q, h_q, 512] bf16 and lse [b, h_q, s_q] fp32 for absorbed queries
     q [b, s_q, h_q, 576] over the paged cache k_cache [pages, 64, 1, 576]."""
-    assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
-    assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
-    b, s_q, h_q, d = q.shape
-    assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and q.stride(1) == h_q * D_QK, \
-        "q rows must be packed: [b][s_q][h_q][576] with the (s_q, h_q) rows contiguous"
-    num_pages, page, h_kv, dk = k_cache.shape
-    assert dk == D_QK and k_cache.stride(3) == 1
-    assert block_table.stride(1) == 1
-    dev = q.device
-    with torch.cuda.device(dev):
-        if out is None:
-            out = torch.empty(b, s_q, h_q, D_V, dtype=torch.bfloat16, device=dev)
-        if lse is None:
-            lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
-        assert out.stride(3) == 1 and lse.is_contiguous()
-        if workspace is None:
-            workspace = torch.empty(workspace_size(b, h_q, s_q, h_kv), dtype=torch.uint8,
-                                    device=dev)
-        cache_seqlens = cache_seqlens.contiguous()
-        st = _lib.load().mla_decode_fwd(
-            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
-            page, _ptr(block_table), block_table.stride(0), block_table.shape[1],
-            _ptr(cache_seqlens), b, s_q, h_q, h_kv, float(softmax_scale), int(bool(causal)),
-            _ptr(meta), _ptr(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-            _ptr(out), out.stride(0), out.stride(1), out.stride(2), _ptr(lse), _stream_ptr(stream))
-        _lib.check(st, "mla_decode_fwd")
-    return out, lse
+    return DecodeCall(q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                      num_splits, workspace, out, lse, stream).fwd()
 
 
 def mla_last_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -190,14 +190,56 @@ int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
     return MLA_OK;
 }
 
-int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
-                   int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
-                   const int32_t* block_table_dev, int64_t bt_batch_stride, int max_blocks_per_seq,
-                   const int32_t* cache_seqlens_dev, int batch, int s_q, int h_q, int h_kv,
-                   float softmax_scale, int causal, const void* meta_dev,
-                   const int32_t* num_splits_dev, void* workspace_dev, size_t workspace_bytes,
-                   void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
-                   int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                 size_t workspace_bytes, int batch, int s_q, int h_q, int h_kv, void* out_dev,
+                 int64_t out_batch_stride, int64_t out_s_stride, int64_t out_h_stride,
+                 float* lse_dev, mla_stream_t stream) {
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    if (!meta_dev || !num_splits_dev || !out_dev || !lse_dev) return MLA_ERR_INVALID_ARGUMENT;
+    if (out_h_stride < kDv || out_s_stride < out_h_stride * h_q ||
+        out_batch_stride < out_s_stride * s_q)
+        return MLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(out_dev) || (out_batch_stride % 8) || (out_s_stride % 8) || (out_h_stride % 8) ||
+        (reinterpret_cast<uintptr_t>(lse_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int R = s_q * h_q;
+    size_t o_bytes = 0, ws_need = 0;
+    workspace_layout(batch, R, num_parts_of(R, d->sms), &o_bytes, &ws_need);
+    if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
+    CombineParams c{};
+    c.meta = static_cast<const int32_t*>(meta_dev);
+    c.num_splits = num_splits_dev;
+    c.oaccum = static_cast<const float*>(workspace_dev);
+    c.lseaccum = reinterpret_cast<const float*>(static_cast<const char*>(workspace_dev) + o_bytes);
+    c.out = static_cast<__nv_bfloat16*>(out_dev);
+    c.out_sb = out_batch_stride;
+    c.out_ss = out_s_stride;
+    c.out_sh = out_h_stride;
+    c.lse = lse_dev;
+    c.batch = batch;
+    c.s_q = s_q;
+    c.h_q = h_q;
+    c.R = R;
+    cudaError_t e = launch_combine(c, reinterpret_cast<cudaStream_t>(stream), /*pdl=*/true);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                 int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
+                 const int32_t* block_table_dev, int64_t bt_batch_stride, int max_blocks_per_seq,
+                 const int32_t* cache_seqlens_dev, int batch, int s_q, int h_q, int h_kv,
+                 float softmax_scale, int causal, const void* meta_dev,
+                 const int32_t* num_splits_dev, void* workspace_dev, size_t workspace_bytes,
+                 void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
     int st = check_shape(batch, h_q, s_q, h_kv);
     if (st) return st;
     if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
@@ -261,26 +303,57 @@ int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cach
     p.error_word = d->error_word;
     p.budget_ns = g_budget_ns.load();
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_decode(p, q_map, kv_map, s);
-    if (e != cudaSuccess) return MLA_ERR_CUDA;
-
-    CombineParams c{};
-    c.meta = p.meta;
-    c.num_splits = num_splits_dev;
-    c.oaccum = p.oaccum;
-    c.lseaccum = p.lseaccum;
-    c.out = p.out;
-    c.out_sb = out_batch_stride;
-    c.out_ss = out_s_stride;
-    c.out_sh = out_h_stride;
-    c.lse = lse_dev;
-    c.batch = batch;
-    c.s_q = s_q;
-    c.h_q = h_q;
-    c.R = R;
-    e = launch_combine(c, s, /*pdl=*/true);
+    cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_splitkv(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                       int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
+                       const int32_t* block_table_dev, int64_t bt_batch_stride,
+                       int max_blocks_per_seq, const int32_t* cache_seqlens_dev, int batch,
+                       int s_q, int h_q, int h_kv, float softmax_scale, int causal,
+                       const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                       size_t workspace_bytes, void* out_dev, int64_t out_batch_stride,
+                       int64_t out_s_stride, int64_t out_h_stride, float* lse_dev,
+                       mla_stream_t stream) {
+    return splitkv_only(q_dev, q_batch_stride, k_cache_dev, k_page_stride, k_token_stride,
+                        num_pages, page_size, block_table_dev, bt_batch_stride, max_blocks_per_seq,
+                        cache_seqlens_dev, batch, s_q, h_q, h_kv, softmax_scale, causal, meta_dev,
+                        num_splits_dev, workspace_dev, workspace_bytes, out_dev, out_batch_stride,
+                        out_s_stride, out_h_stride, lse_dev, stream);
+}
+
+int mla_decode_combine(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                       size_t workspace_bytes, int batch, int s_q, int h_q, int h_kv,
+                       void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                       int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+    return combine_only(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, s_q, h_q,
+                        h_kv, out_dev, out_batch_stride, out_s_stride, out_h_stride, lse_dev,
+                        stream);
+}
+
+int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                   int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
+                   const int32_t* block_table_dev, int64_t bt_batch_stride, int max_blocks_per_seq,
+                   const int32_t* cache_seqlens_dev, int batch, int s_q, int h_q, int h_kv,
+                   float softmax_scale, int causal, const void* meta_dev,
+                   const int32_t* num_splits_dev, void* workspace_dev, size_t workspace_bytes,
+                   void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                   int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+    int st = splitkv_only(q_dev, q_batch_stride, k_cache_dev, k_page_stride, k_token_stride,
+                          num_pages, page_size, block_table_dev, bt_batch_stride,
+                          max_blocks_per_seq, cache_seqlens_dev, batch, s_q, h_q, h_kv,
+                          softmax_scale, causal, meta_dev, num_splits_dev, workspace_dev,
+                          workspace_bytes, out_dev, out_batch_stride, out_s_stride, out_h_stride,
+                          lse_dev, stream);
+    if (st) return st;
+    return combine_only(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, s_q, h_q,
+                        h_kv, out_dev, out_batch_stride, out_s_stride, out_h_stride, lse_dev,
+                        stream);
 }
 
 int mla_last_device_error(mla_stream_t stream, int* code) {

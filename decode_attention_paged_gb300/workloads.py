@@ -92,33 +92,37 @@ def make(name: str, b: int, s_q: int, h_q: int, seqlens: Sequence[int], num_page
     return Workload(name, q, k_cache, block_table.to(torch.int32), seqlens, scale, causal)
 
 
-def tiny() -> Workload:
+def tiny(seed_offset: int = 0) -> Workload:
     """batch 1, s_q 1, h_q 16, 4 pages, identity block table, L = 256, non-causal."""
     bt = torch.arange(4, dtype=torch.int32).view(1, 4)
-    return make("tiny b1 s_q1 h_q16 L256", 1, 1, 16, [256], 4, 4, block_table=bt)
+    return make("tiny b1 s_q1 h_q16 L256", 1, 1, 16, [256], 4, 4, block_table=bt,
+                seed_offset=seed_offset)
 
 
-def memory_bound() -> Workload:
+def memory_bound(seed_offset: int = 0) -> Workload:
     """batch 64, s_q 1, h_q 16, every L = 4096, 4096 pages permuted."""
-    return make("memory-bound b64 s_q1 h_q16 L4096", 64, 1, 16, [4096] * 64, 4096, 64)
+    return make("memory-bound b64 s_q1 h_q16 L4096", 64, 1, 16, [4096] * 64, 4096, 64,
+                seed_offset=seed_offset)
 
 
-def compute_bound() -> Workload:
+def compute_bound(seed_offset: int = 0) -> Workload:
     """batch 64, s_q 1, h_q 128, L ~ U[1, 8192] (seed 4), 64*128 pages permuted."""
-    L = torch.randint(1, 8193, (64,), generator=_gen(4), dtype=torch.int64).tolist()
-    return make("compute-bound b64 s_q1 h_q128 L~U[1,8192]", 64, 1, 128, L, 64 * 128, 128)
+    L = torch.randint(1, 8193, (64,), generator=_gen(4 + seed_offset), dtype=torch.int64).tolist()
+    return make("compute-bound b64 s_q1 h_q128 L~U[1,8192]", 64, 1, 128, L, 64 * 128, 128,
+                seed_offset=seed_offset)
 
 
-def mtp() -> Workload:
+def mtp(seed_offset: int = 0) -> Workload:
     """batch 128, s_q 2, h_q 128, causal within the 2 query tokens, L = 4096."""
     return make("MTP b128 s_q2 h_q128 causal L4096", 128, 2, 128, [4096] * 128, 8192, 64,
-                causal=True)
+                causal=True, seed_offset=seed_offset)
 
 
-def long_ragged() -> Workload:
+def long_ragged(seed_offset: int = 0) -> Workload:
     """batch 8, s_q 1, h_q 64, L = 1 .. 65536, 8192 pages, 1024 blocks per row."""
     L = [1, 64, 1000, 8191, 16384, 32768, 49152, 65536]
-    return make("long ragged b8 s_q1 h_q64 L<=65536", 8, 1, 64, L, 8192, 1024)
+    return make("long ragged b8 s_q1 h_q64 L<=65536", 8, 1, 64, L, 8192, 1024,
+                seed_offset=seed_offset)
 
 
 CONFIGS = {

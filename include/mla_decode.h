@@ -161,6 +161,39 @@ MLA_API int mla_decode_fwd(const void *q_dev, int64_t q_batch_stride, const void
                    int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
 
 /*
+ * mla_decode_splitkv / mla_decode_combine -- the two kernels mla_decode_fwd
+ * enqueues, callable one at a time (the split-KV kernel and the combine kernel
+ * of "FlashMLA 新内核深度解析", section "Programmatic Dependent Launch").
+ * mla_decode_fwd(args) is exactly mla_decode_splitkv(args) followed by
+ * mla_decode_combine(...) on the same stream; separately they let a caller
+ * place events between the two (e.g. to time each kernel).
+ *
+ * mla_decode_splitkv takes mla_decode_fwd's arguments and has the same
+ * checks and errors.  It writes out/lse of every request the plan kept in one
+ * piece, and the partial results of split requests into the workspace.
+ *
+ * mla_decode_combine merges the partials of split requests into out/lse.
+ * Arguments have the meaning they have in mla_decode_fwd; workspace_dev must
+ * hold the partials the matching mla_decode_splitkv call wrote.  It is
+ * launched as a programmatic dependent of the preceding kernel on `stream`.
+ */
+MLA_API int mla_decode_splitkv(const void *q_dev, int64_t q_batch_stride, const void *k_cache_dev,
+                               int64_t k_page_stride, int64_t k_token_stride, int num_pages,
+                               int page_size, const int32_t *block_table_dev,
+                               int64_t bt_batch_stride, int max_blocks_per_seq,
+                               const int32_t *cache_seqlens_dev, int batch, int s_q, int h_q,
+                               int h_kv, float softmax_scale, int causal, const void *meta_dev,
+                               const int32_t *num_splits_dev, void *workspace_dev,
+                               size_t workspace_bytes, void *out_dev, int64_t out_batch_stride,
+                               int64_t out_s_stride, int64_t out_h_stride, float *lse_dev,
+                               mla_stream_t stream);
+MLA_API int mla_decode_combine(const void *meta_dev, const int32_t *num_splits_dev,
+                               void *workspace_dev, size_t workspace_bytes, int batch, int s_q,
+                               int h_q, int h_kv, void *out_dev, int64_t out_batch_stride,
+                               int64_t out_s_stride, int64_t out_h_stride, float *lse_dev,
+                               mla_stream_t stream);
+
+/*
  * mla_last_device_error -- synchronise `stream`, then read and clear the
  * current device's error word.  *code receives MLA_OK or the first device-side
  * MLA_ERR_* recorded since the last call.  Returns MLA_ERR_CUDA if the
