@@ -41,6 +41,8 @@ SIGNATURES = {
     "mla_decode_splitkv": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I,
                                 _F, _I, _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P, _P]),
     "mla_decode_combine": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _P, _I64, _I64, _I64, _P, _P]),
+    "mla_decode_fwd_noalloc": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I,
+                                    _I, _I, _F, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
     "mla_last_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "mla_set_wait_budget_ns": (_I, [ctypes.c_uint64]),
     "mla_set_fixed_overhead": (_I, [_I]),

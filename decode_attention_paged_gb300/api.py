@@ -138,6 +138,31 @@ def mla_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Te
                       num_splits, workspace, out, lse, stream).fwd()
 
 
+def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
+                           cache_seqlens: torch.Tensor, softmax_scale: float, causal: bool,
+                           meta: torch.Tensor, num_splits: torch.Tensor, out: torch.Tensor,
+                           lse: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """mla_decode_fwd for callers that cannot allocate device memory: the
+    library supplies the split-KV scratch from a fixed 32 MiB device array
+    (see include/mla_decode.h).  The caller passes out and lse; nothing here
+    allocates."""
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+    b, s_q, h_q, d = q.shape
+    assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and q.stride(1) == h_q * D_QK
+    num_pages, page, h_kv, dk = k_cache.shape
+    assert dk == D_QK and k_cache.stride(3) == 1 and block_table.stride(1) == 1
+    assert out.stride(3) == 1 and lse.is_contiguous() and cache_seqlens.is_contiguous()
+    with torch.cuda.device(q.device):
+        st = _lib.load().mla_decode_fwd_noalloc(
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
+            page, _ptr(block_table), block_table.stride(0), block_table.shape[1],
+            _ptr(cache_seqlens), b, s_q, h_q, h_kv, float(softmax_scale), int(bool(causal)),
+            _ptr(meta), _ptr(num_splits), _ptr(out), out.stride(0), out.stride(1), out.stride(2),
+            _ptr(lse), _stream_ptr(stream))
+        _lib.check(st, "mla_decode_fwd_noalloc")
+    return out, lse
+
+
 def mla_last_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and read/clear the device error word."""
     code = ctypes.c_int()

@@ -194,6 +194,50 @@ MLA_API int mla_decode_combine(const void *meta_dev, const int32_t *num_splits_d
                                mla_stream_t stream);
 
 /*
+ * mla_decode_fwd_noalloc -- mla_decode_fwd for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a service of this
+ * library.
+ *
+ * Who needs it.  Some callers may not call cudaMalloc (or any allocator) at
+ * the point where they decode:
+ *   - a plugin inside a host framework that owns the whole device memory pool
+ *     and hands the plugin no allocator;
+ *   - a serving loop that forbids device allocation on its hot path, because
+ *     cudaMalloc can synchronise the device and stall every other stream;
+ *   - a process that has already reserved device memory up to its limit.
+ * They still own and pass every input and output; only the split-KV scratch
+ * (the `workspace` of mla_decode_fwd) is supplied by the library.
+ *
+ * Arguments and results are those of mla_decode_fwd without workspace_dev and
+ * workspace_bytes.  The scratch is one static device array of
+ * MLA_NOALLOC_SCRATCH_BYTES (32 MiB) inside libmla.so: every GPU that loads
+ * the library keeps those 32 MiB until the process exits.  A problem whose
+ * mla_workspace_size() exceeds it is refused with MLA_ERR_WORKSPACE_TOO_SMALL
+ * before anything is enqueued (e.g. batch 64 x h_q 16 needs ~7 MB and fits;
+ * batch 64 x h_q 128 needs ~37 MB and does not).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps whatever
+ * the last call left there; nothing in it needs to start at zero, because
+ * every partial the combine reads is written earlier by the same call.  Calls
+ * whose work overlaps on the GPU (e.g. on two streams at once) race on the
+ * array and give wrong results: serialise them.  Allocates nothing and calls
+ * no allocating routine.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+MLA_API int mla_decode_fwd_noalloc(const void *q_dev, int64_t q_batch_stride,
+                                   const void *k_cache_dev, int64_t k_page_stride,
+                                   int64_t k_token_stride, int num_pages, int page_size,
+                                   const int32_t *block_table_dev, int64_t bt_batch_stride,
+                                   int max_blocks_per_seq, const int32_t *cache_seqlens_dev,
+                                   int batch, int s_q, int h_q, int h_kv, float softmax_scale,
+                                   int causal, const void *meta_dev,
+                                   const int32_t *num_splits_dev, void *out_dev,
+                                   int64_t out_batch_stride, int64_t out_s_stride,
+                                   int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
+
+/*
  * mla_last_device_error -- synchronise `stream`, then read and clear the
  * current device's error word.  *code receives MLA_OK or the first device-side
  * MLA_ERR_* recorded since the last call.  Returns MLA_ERR_CUDA if the
