@@ -74,7 +74,8 @@ int num_parts_of(int R, int sms) {
 }
 
 int check_shape(int batch, int h_q, int s_q, int h_kv) {
-    if (batch < 1 || h_q < 1 || s_q < 1 || batch > 65535) return MLA_ERR_INVALID_ARGUMENT;
+    if (batch < 1 || h_q < 1 || s_q < 1) return MLA_ERR_INVALID_ARGUMENT;
+    if (batch > sched_max_batch()) return MLA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(s_q) * h_q > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
     return MLA_OK;
@@ -144,7 +145,7 @@ int mla_set_wait_budget_ns(uint64_t budget_ns) {
 }
 
 int mla_set_fixed_overhead(int blocks) {
-    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead : blocks);
+    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead : (blocks < 1 ? 1 : blocks));
     return MLA_OK;
 }
 
@@ -165,7 +166,7 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
     int st = check_shape(batch, h_q, s_q, h_kv);
     if (st) return st;
     if (!cache_seqlens_dev || !meta_dev || !num_splits_dev) return MLA_ERR_INVALID_ARGUMENT;
-    if ((reinterpret_cast<uintptr_t>(meta_dev) & 3u) || (reinterpret_cast<uintptr_t>(num_splits_dev) & 3u) ||
+    if ((reinterpret_cast<uintptr_t>(meta_dev) & 15u) || (reinterpret_cast<uintptr_t>(num_splits_dev) & 3u) ||
         (reinterpret_cast<uintptr_t>(cache_seqlens_dev) & 3u))
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;

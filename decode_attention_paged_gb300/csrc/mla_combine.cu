@@ -8,7 +8,7 @@
 // cudaGridDependencySynchronize (griddepcontrol.wait) and reads the partials
 // with ordinary loads (not the read-only path, which does not see the
 // producer's writes under programmatic launch).  Pieces whose lse is -inf
-// (nothing visible) get weight 0; if every piece is empty the row is 0 and
+// (nothing visible) get weight 0 (their partial rows are written as zeros); if every piece is empty the row is 0 and
 // lse -inf ("CUTLASS 从零重写 FlashAttention：Split KV 并行优化实战", sec. 3.3).
 //
 // Layout: oaccum [pieces][R][512] fp32 holds each piece's normalised output,
@@ -78,19 +78,44 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
-    for (int k = 0; k < n; ++k) {
-        const float lk = ld_f(lse_base + static_cast<int64_t>(k) * p.R);
-        const float w = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
-        if (w == 0.f) continue;  // never touch an empty piece's (unwritten) output
-        wsum += w;
-        const float* src = o_base + static_cast<int64_t>(k) * p.R * kDv;
+    const int64_t piece_stride = static_cast<int64_t>(p.R) * kDv;
+    // Lane k of each group of 32 pieces holds piece k's weight; the partial
+    // rows are then streamed with all loads of a group of four in flight.
+    // An empty piece (lse = -inf) has weight 0 and an all-zero partial row.
+    for (int base = 0; base < n; base += 32) {
+        const int k = base + lane;
+        const float lk = k < n ? ld_f(lse_base + static_cast<int64_t>(k) * p.R) : -INFINITY;
+        const float wl = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
+        float ws = wl;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            float4 x = ld_f4(src + 4 * v);
-            acc[4 * v + 0] += w * x.x;
-            acc[4 * v + 1] += w * x.y;
-            acc[4 * v + 2] += w * x.z;
-            acc[4 * v + 3] += w * x.w;
+        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        wsum += ws;
+        const int m = min(32, n - base);
+        for (int j0 = 0; j0 < m; j0 += 4) {
+            float4 x[4][4];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                w[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
+                if (j0 + u < m) {
+                    const float* src = o_base + static_cast<int64_t>(base + j0 + u) * piece_stride;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) x[u][v] = ld_f4(src + 4 * v);
+                } else {
+                    w[u] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    acc[4 * v + 0] += w[u] * x[u][v].x;
+                    acc[4 * v + 1] += w[u] * x[u][v].y;
+                    acc[4 * v + 2] += w[u] * x[u][v].z;
+                    acc[4 * v + 3] += w[u] * x[u][v].w;
+                }
         }
     }
     const float inv = 1.f / wsum;

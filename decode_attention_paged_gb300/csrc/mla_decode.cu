@@ -60,24 +60,35 @@ constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
 // own, so the drain has its own budget, independent of the (possibly tiny)
 // wait budget a caller set.
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+#ifndef MLA_PREFETCH_PAGES
+#define MLA_PREFETCH_PAGES 0
+#endif
+// L2 prefetch distance in pages.  Off by default: measured on GB300, a 2-page
+// TMA ring already streams at the HBM limit and extra L2 prefetches only add
+// traffic; the read-ahead of block-table entries below is kept either way.
+constexpr uint32_t kPrefetchPages = MLA_PREFETCH_PAGES;
+constexpr uint32_t kReadAhead = 8;      // block-table entries read ahead of the loads
+constexpr int kPageRing = 16;           // ring of those entries (> kReadAhead)
+static_assert(kPrefetchPages <= kReadAhead && kReadAhead < kPageRing, "read-ahead ring");
 
 struct Barriers {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full, q_empty;
     uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, pv_done, o_free, grp, drain;
+    uint64_t p_full, pv_done, o_free, drain;
 };
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffBar = kOffP + kPBytes;
-constexpr uint32_t kOffRedMax = kOffBar + 256;          // float [2][128]
-constexpr uint32_t kOffRedL = kOffRedMax + 2 * 128 * 4;  // float [2][128]
-constexpr uint32_t kOffMisc = kOffRedL + 2 * 128 * 4;    // tmem base, abort flag
+constexpr uint32_t kOffXch = kOffBar + 256;            // uint2 [2][128]: pair exchange
+constexpr uint32_t kOffMisc = kOffXch + 2 * 128 * 8;    // tmem base, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 static_assert(sizeof(Barriers) <= 256, "barrier block");
+static_assert(kChunks % 3 == 0, "QK^T is issued three chunks per turn");
+static_assert(kSmemBytes < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 struct Part {
@@ -103,6 +114,41 @@ __device__ __forceinline__ void item_range(const DecodeParams& p, const Part& pa
     if (b0 > b1) b0 = b1;
 }
 
+// A walk over the (request, block) work items of one part, in order.  Each
+// role keeps its own cursors; all walk the same sequence.
+struct Cursor {
+    int req, blk, b0, b1, L, nb;
+    uint32_t g;     // block index within the part's work
+    uint32_t item;  // index of the current request among those with blocks
+    bool valid;
+};
+__device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& part, Cursor& c,
+                                            int req) {
+    for (; req <= part.end_req; ++req) {
+        item_range(p, part, req, c.L, c.nb, c.b0, c.b1);
+        if (c.b1 > c.b0) {
+            c.req = req;
+            c.blk = c.b0;
+            c.valid = true;
+            return;
+        }
+    }
+    c.valid = false;
+}
+__device__ __forceinline__ Cursor cursor_begin(const DecodeParams& p, const Part& part) {
+    Cursor c;
+    c.g = 0;
+    c.item = 0;
+    cursor_seek(p, part, c, part.begin_req);
+    return c;
+}
+__device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& part, Cursor& c) {
+    ++c.g;
+    if (++c.blk < c.b1) return;
+    ++c.item;
+    cursor_seek(p, part, c, c.req + 1);
+}
+
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
     bool ok = true;
@@ -120,6 +166,51 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
     }
 }
 
+// Exchange one float with the partner thread that holds the other half of
+// the same query row (TMEM lane L <-> L ^ 64).  Each side publishes (value,
+// tag) with one 64-bit store and spins, with a bounded wait, until the
+// partner's slot carries the same tag.  Two slots alternate: a thread can be at
+// most one exchange ahead of its partner, because it cannot finish exchange
+// n + 1 before the partner has published it.  The verdict is made uniform
+// across the warp, so warp-collective instructions stay convergent.
+__device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& seq, float v,
+                                              float& partner, const WaitCtx& wc) {
+    const uint32_t tag = ++seq;
+    uint2* slots = xch + (tag & 1) * 128;
+    asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(slots + lrow)),
+                 "r"(__float_as_uint(v)), "r"(tag)
+                 : "memory");
+    const uint32_t src = smem_u32(slots + (lrow ^ 64));
+    auto load = [&]() {
+        uint2 r;
+        asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(src)
+                     : "memory");
+        return r;
+    };
+    bool ok = true;
+    uint2 got = load();
+    if (got.y != tag) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+            got = load();
+            if (got.y == tag) break;
+            if ((spin & 255) == 0) {
+                if (*wc.abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > wc.budget_ns) {
+                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    partner = __uint_as_float(got.x);
+    return __all_sync(0xffffffffu, ok);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -133,8 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sKV = smem + kOffKV;
     uint8_t* sP = smem + kOffP;
     Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
-    float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
-    float* red_l = reinterpret_cast<float*>(smem + kOffRedL);
+    uint2* xch = reinterpret_cast<uint2*>(smem + kOffXch);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
@@ -155,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->p_full, 4);
         mbar_init(&bars->pv_done, 1);
         mbar_init(&bars->o_free, 4);
-        mbar_init(&bars->grp, 4);
         mbar_init(&bars->drain, 1);
         fence_barrier_init();
         prefetch_tensormap(&q_map);
@@ -165,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // Pair-exchange slots start with tag 0, which no exchange uses.
+    for (int i = tid; i < 2 * 128; i += kThreads) xch[i] = make_uint2(0u, 0u);
     // Query rows a partial Q tile load does not bring must read as zeros.
     if (p.q_box_rows < kTileM) {
         for (int i = tid; i < kChunks * kTileM * 8; i += kThreads) {
@@ -216,114 +307,148 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ TMA producer
+        // Loads run through a two-page ring; a second cursor kReadAhead pages
+        // ahead reads the block table early, so a load never waits for its
+        // page index (and, if kPrefetchPages > 0, asks L2 to fetch upcoming
+        // pages and the next request's Q tile).
         const uint64_t policy = policy_evict_first();
-        uint32_t g = 0, n_items = 0;
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
-        for (int req = part.begin_req; req <= part.end_req; ++req) {
-            int L, nb, b0, b1;
-            item_range(p, part, req, L, nb, b0, b1);
-            if (b1 <= b0) continue;
-            if (n_items > 0 && !mbar_wait(&bars->q_empty, (n_items - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
-                break;
-            mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-            for (int c = 0; c < kChunks; ++c)
-                tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c, mtile * kTileM,
-                            req, policy);
-            ++n_items;
-            bool stop = false;
-            for (int blk = b0; blk < b1; ++blk, ++g) {
-                const int st = g & 1;
-                if (g >= 2 && !mbar_wait(&bars->kv_empty[st], ((g >> 1) + 1) & 1, wc,
-                                         MLA_ERR_DEVICE_TIMEOUT)) {
-                    stop = true;
-                    break;
-                }
-                const int page = p.block_table[static_cast<int64_t>(req) * p.bt_stride + blk];
-                mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                uint8_t* dst = sKV + st * kStageBytes;
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
-                                policy);
+        Cursor ld = cursor_begin(p, part), pf = ld;
+        int ring[kPageRing];
+        uint32_t n_kv = 0, n_q = 0;
+        while (ld.valid) {
+            while (pf.valid && pf.g <= ld.g + kReadAhead) {
+                const int page = p.block_table[static_cast<int64_t>(pf.req) * p.bt_stride + pf.blk];
+                ring[pf.g % kPageRing] = page;
+                if (pf.g > ld.g && pf.g <= ld.g + kPrefetchPages)
+                    for (int c = 0; c < kChunks; ++c) tma_prefetch_l2_3d(&kv_map, 64 * c, 0, page);
+                if (kPrefetchPages > 0 && pf.blk == pf.b0 && pf.item > ld.item)
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_prefetch_l2_3d(&q_map, 64 * c, mtile * kTileM, pf.req);
+                cursor_next(p, part, pf);
             }
-            if (stop) break;
+            const int st = ld.g & 1;
+            if (ld.g >= 2 &&
+                !mbar_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
+                break;
+            const int page = ring[ld.g % kPageRing];
+            mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+            uint8_t* dst = sKV + st * kStageBytes;
+            for (int c = 0; c < kChunks; ++c)
+                tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
+                            policy);
+            ++n_kv;
+            if (ld.blk == ld.b0) {  // first block of a request: its Q tile
+                if (ld.item > 0 &&
+                    !mbar_wait(&bars->q_empty, (ld.item - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
+                    break;
+                mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
+                                mtile * kTileM, ld.req, policy);
+                ++n_q;
+            }
+            cursor_next(p, part, ld);
         }
         // Drain: never leave the CTA with copies still landing in its smem.
-        for (uint32_t k = (g >= 2 ? g - 2 : 0); k < g; ++k)
+        for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)
             mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
-        if (n_items > 0) mbar_drain(&bars->q_full, (n_items - 1) & 1, kDrainBudgetNs);
+        if (n_q > 0) mbar_drain(&bars->q_full, (n_q - 1) & 1, kDrainBudgetNs);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer
+        // Two cursors: QK^T of block g needs its page, its request's Q tile
+        // and a free S buffer; PV of block g needs P(g) from the softmax warps
+        // (and, on a request's first block, O released by the previous
+        // request's epilogue).  The thread polls without blocking and issues
+        // QK^T one 64-dim chunk (4 MMAs) at a time, checking for a ready PV
+        // between chunks: a PV never waits behind a whole QK^T, so the stage
+        // it frees goes back to the producer as early as possible.
         constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
-        const uint32_t sQ_a = smem_u32(sQ), sKV_a = smem_u32(sKV), sP_a = smem_u32(sP);
-        uint32_t g = 0, n_items = 0;
-        bool pend = false, pend_first = false;
-        uint32_t pend_g = 0, pend_item = 0;
-        bool alive = true;
-        auto issue_pv = [&](uint32_t pg, bool first_of_item, uint32_t item) -> bool {
-            if (!mbar_wait(&bars->p_full, pg & 1, wc, MLA_ERR_DEVICE_TIMEOUT)) return false;
-            if (first_of_item && item > 0 &&
-                !mbar_wait(&bars->o_free, (item - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
-                return false;
-            tc_fence_after();
-            const uint32_t v_base = sKV_a + (pg & 1) * kStageBytes;
+        // Descriptors are built once; an MMA's operand then differs only in
+        // the start-address field (bits 0..13, 16-byte units), which a plain
+        // add moves without carrying into the next field (every address here
+        // is below 256 KB).
+        const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024);
+        const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024);
+        const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
+        const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024);
+        constexpr uint64_t kStageUnits = kStageBytes >> 4;
+        constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
+        Cursor qk = cursor_begin(p, part), pv = qk;
+        int qk_chunk = 0;  // next 64-dim chunk of QK^T(qk.g) to issue; 0 = not started
+        uint64_t idle_since = 0;
+        uint32_t idle_spins = 0;
+        while (pv.valid) {
+            bool did = false;
+            if (pv.g < qk.g) {
+                const bool first = pv.blk == pv.b0;
+                bool ready = mbar_test_wait(&bars->p_full, pv.g & 1);
+                if (ready && first && pv.item > 0)
+                    ready = mbar_test_wait(&bars->o_free, (pv.item - 1) & 1);
+                if (ready) {
+                    tc_fence_after();
+                    const uint64_t dV = dV0 + (pv.g & 1) * kStageUnits;
+                    const uint32_t d0 = tmem + kColO, d1 = tmem + kColO + 128;
+                    mma_ws_ss(d0, dP, dV, idesc_pv, first ? 0u : 1u);
+                    mma_ws_ss(d1, dP, dV + 4 * kChunkUnits, idesc_pv, first ? 0u : 1u);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = smem_desc(sP_a + kk * 32, 16, 1024);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint64_t b = smem_desc(v_base + h * 4 * kChunkBytes + kk * 2048,
-                                                 kChunkBytes, 1024);
-                    mma_ws_ss(tmem + kColO + 128 * h, a, b, idesc_pv,
-                              (first_of_item && kk == 0) ? 0u : 1u);
-                }
-            }
-            mma_commit(&bars->pv_done);
-            mma_commit(&bars->kv_empty[pg & 1]);
-            return true;
-        };
-        for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
-            int L, nb, b0, b1;
-            item_range(p, part, req, L, nb, b0, b1);
-            if (b1 <= b0) continue;
-            if (!mbar_wait(&bars->q_full, n_items & 1, wc, MLA_ERR_DEVICE_TIMEOUT)) {
-                alive = false;
-                break;
-            }
-            for (int blk = b0; blk < b1; ++blk, ++g) {
-                const int st = g & 1;
-                if (!mbar_wait(&bars->kv_full[st], (g >> 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT) ||
-                    (g >= 2 && !mbar_wait(&bars->s_empty[st], ((g >> 1) + 1) & 1, wc,
-                                          MLA_ERR_DEVICE_TIMEOUT))) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t k_base = sKV_a + st * kStageBytes;
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = smem_desc(sQ_a + c * kChunkBytes + kk * 32, 16, 1024);
-                        const uint64_t b = smem_desc(k_base + c * kChunkBytes + kk * 32, 16, 1024);
-                        mma_ws_ss(tmem + kColS + 32 * st, a, b, idesc_qk, (c | kk) ? 1u : 0u);
+                    for (int kk = 1; kk < 4; ++kk) {
+                        mma_ws_ss(d0, dP + 2 * kk, dV + 128 * kk, idesc_pv, 1u);
+                        mma_ws_ss(d1, dP + 2 * kk, dV + 4 * kChunkUnits + 128 * kk, idesc_pv, 1u);
                     }
+                    mma_commit(&bars->pv_done);
+                    mma_commit(&bars->kv_empty[pv.g & 1]);
+                    cursor_next(p, part, pv);
+                    did = true;
                 }
-                mma_commit(&bars->s_full[st]);
-                if (blk == b1 - 1) mma_commit(&bars->q_empty);
-                if (pend && !issue_pv(pend_g, pend_first, pend_item)) {
-                    alive = false;
-                    pend = false;
+            }
+            if (qk.valid) {
+                const int st = qk.g & 1;
+                bool ready = true;
+                if (qk_chunk == 0) {
+                    if (qk.blk == qk.b0) ready = mbar_test_wait(&bars->q_full, qk.item & 1);
+                    ready = ready && mbar_test_wait(&bars->kv_full[st], (qk.g >> 1) & 1);
+                    if (ready && qk.g >= 2)
+                        ready = mbar_test_wait(&bars->s_empty[st], ((qk.g >> 1) + 1) & 1);
+                    if (ready) tc_fence_after();
+                }
+                if (ready) {
+                    // Three 64-dim chunks (12 MMAs) per turn, then look for a ready PV.
+                    const uint32_t dS = tmem + kColS + 32 * st;
+                    const uint64_t dK = dK0 + st * kStageUnits;
+                    const int c_end = qk_chunk + 3;
+                    for (int c = qk_chunk; c < c_end; ++c) {
+                        const uint64_t a = dQ + c * kChunkUnits, b = dK + c * kChunkUnits;
+                        mma_ws_ss(dS, a, b, idesc_qk, c ? 1u : 0u);
+                        mma_ws_ss(dS, a + 2, b + 2, idesc_qk, 1u);
+                        mma_ws_ss(dS, a + 4, b + 4, idesc_qk, 1u);
+                        mma_ws_ss(dS, a + 6, b + 6, idesc_qk, 1u);
+                    }
+                    qk_chunk = c_end;
+                    if (qk_chunk == kChunks) {
+                        qk_chunk = 0;
+                        mma_commit(&bars->s_full[st]);
+                        if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
+                        cursor_next(p, part, qk);
+                    }
+                    did = true;
+                }
+            }
+            if (did) {
+                idle_since = 0;
+                idle_spins = 0;
+            } else if ((++idle_spins & 63) == 0) {
+                if (*abort_flag) break;
+                const uint64_t now = globaltimer_ns();
+                if (idle_since == 0) {
+                    idle_since = now;
+                } else if (now - idle_since > p.budget_ns) {
+                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
                     break;
                 }
-                pend = true;
-                pend_g = g;
-                pend_first = (blk == b0);
-                pend_item = n_items;
             }
-            ++n_items;
         }
-        if (alive && pend) issue_pv(pend_g, pend_first, pend_item);
         // Drain: all MMAs finished before TMEM is released.
         mma_commit(&bars->drain);
         mbar_drain(&bars->drain, 0, kDrainBudgetNs);
@@ -336,14 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = row < p.R;
         const int s_idx = row / p.h_q, h_idx = row % p.h_q;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-        uint32_t gblk = 0, n_items = 0, grp_phase = 0;
+        uint32_t gblk = 0, n_items = 0, xseq = 0;
         bool alive = true;
-        auto group_sync = [&]() -> bool {
-            warp_arrive(&bars->grp);
-            const bool okw = warp_wait(&bars->grp, grp_phase & 1, wc);
-            ++grp_phase;
-            return okw;
-        };
         for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
             int L, nb, b0, b1;
             item_range(p, part, req, L, nb, b0, b1);
@@ -377,12 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x[c] = (t0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
                     hmax = fmaxf(hmax, x[c]);
                 }
-                red_max[(gblk & 1) * 128 + Lrow] = hmax;
-                if (!group_sync()) {
+                float pmax;
+                if (!pair_exchange(xch, Lrow, xseq, hmax, pmax, wc)) {
                     alive = false;
                     break;
                 }
-                const float tmax = fmaxf(hmax, red_max[(gblk & 1) * 128 + (Lrow ^ 64)]);
+                const float tmax = fmaxf(hmax, pmax);
                 float alpha = 1.f;
                 bool need = false;
                 if (tmax > m_used + kLazyThreshold) {
@@ -455,12 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                red_l[(n_items & 1) * 128 + Lrow] = l_part;
-                if (!group_sync()) {
+                float l_other;
+                if (!pair_exchange(xch, Lrow, xseq, l_part, l_other, wc)) {
                     alive = false;
                     break;
                 }
-                l_tot = l_part + red_l[(n_items & 1) * 128 + (Lrow ^ 64)];
+                l_tot = l_part + l_other;
             }
             const bool empty = !(l_tot > 0.f);
             const float inv = empty ? 0.f : 1.f / l_tot;

@@ -82,5 +82,6 @@ cudaError_t launch_sched(const int32_t* seqlens, int batch, int R, int num_parts
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+int sched_max_batch();
 
 }  // namespace mla

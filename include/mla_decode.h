@@ -36,7 +36,8 @@
  *     exceeded its time budget) are recorded in a per-device error word and
  *     reported by mla_last_device_error().
  * Supported: bf16 q / k_cache / out, fp32 lse, h_kv = 1, d_qk = 576,
- * d_v = 512, page size 64, GPUs of compute capability 10.3 (GB300).
+ * d_v = 512, page size 64, batch <= 16384, GPUs of compute capability 10.3
+ * (GB300); other shapes return MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -101,7 +102,7 @@ MLA_API int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t *met
  * greedily, splitting a request over parts when it does not fit).
  *   cache_seqlens_dev : int32[batch], device.  Negative values count as 0.
  *   meta_dev          : device buffer of mla_metadata_size() meta_bytes,
- *                       4-byte aligned; receives header + part records.
+ *                       16-byte aligned; receives header + part records.
  *   num_splits_dev    : device int32[batch + 1]; receives the prefix sum of the
  *                       number of pieces each request is cut into.
  * The plan is valid for mla_decode_fwd calls with the same batch, s_q, h_q,
@@ -256,8 +257,8 @@ MLA_API int mla_set_wait_budget_ns(uint64_t budget_ns);
 /*
  * mla_set_fixed_overhead -- the scheduler's fixed per-piece overhead in
  * 64-token blocks (fixed_overhead_num_blocks in the "Tile Scheduler" section;
- * default 2).  Affects only load balance, never results.  Process-wide;
- * negative restores the default.
+ * default 2, at least 1: 0 is raised to 1).  Affects only load balance, never
+ * results.  Process-wide; negative restores the default.
  */
 MLA_API int mla_set_fixed_overhead(int blocks);
 
