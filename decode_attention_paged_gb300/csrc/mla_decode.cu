@@ -67,6 +67,19 @@ constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 // TMA ring already streams at the HBM limit and extra L2 prefetches only add
 // traffic; the read-ahead of block-table entries below is kept either way.
 constexpr uint32_t kPrefetchPages = MLA_PREFETCH_PAGES;
+#ifndef MLA_MMA_STRICT
+#define MLA_MMA_STRICT 0
+#endif
+// 1: QK^T of block g + 1 is issued only after PV of block g.
+constexpr bool kStrictOrder = MLA_MMA_STRICT != 0;
+#ifndef MLA_IDLE_SLEEP_NS
+#define MLA_IDLE_SLEEP_NS 32
+#endif
+constexpr unsigned kIdleSleepNs = MLA_IDLE_SLEEP_NS;  // MMA issuer back-off when idle
+#ifndef MLA_XCH_SLEEP_NS
+#define MLA_XCH_SLEEP_NS 32
+#endif
+constexpr unsigned kXchSleepNs = MLA_XCH_SLEEP_NS;  // pair-exchange back-off
 constexpr uint32_t kReadAhead = 8;      // block-table entries read ahead of the loads
 constexpr int kPageRing = 16;           // ring of those entries (> kReadAhead)
 static_assert(kPrefetchPages <= kReadAhead && kReadAhead < kPageRing, "read-ahead ring");
@@ -192,6 +205,9 @@ __device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& se
     if (got.y != tag) {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t spin = 1;; ++spin) {
+            // Back off: a hot spin of 32 lanes on shared memory would eat the
+            // bandwidth the tensor core needs to read its operands.
+            __nanosleep(kXchSleepNs);
             got = load();
             if (got.y == tag) break;
             if ((spin & 255) == 0) {
@@ -209,6 +225,22 @@ __device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& se
     }
     partner = __uint_as_float(got.x);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Chunks [C0, C0 + 3) of S = Q K^T for one page: 12 MMAs, each issued by one
+// elected lane of the converged warp, operand offsets known at compile time.
+template <int C0>
+__device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t d) {
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
+    constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
+#pragma unroll
+    for (int cc = 0; cc < 3; ++cc) {
+        const uint64_t a = dQ + (C0 + cc) * kChunkUnits, b = bK + (C0 + cc) * kChunkUnits;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            if (elect_one()) mma_ws_ss(d, a + 2 * kk, b + 2 * kk, idesc_qk, (C0 + cc + kk) ? 1u : 0u);
+        }
+    }
 }
 
 }  // namespace
@@ -354,16 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)
             mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
         if (n_q > 0) mbar_drain(&bars->q_full, (n_q - 1) & 1, kDrainBudgetNs);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         // Two cursors: QK^T of block g needs its page, its request's Q tile
         // and a free S buffer; PV of block g needs P(g) from the softmax warps
         // (and, on a request's first block, O released by the previous
-        // request's epilogue).  The thread polls without blocking and issues
-        // QK^T one 64-dim chunk (4 MMAs) at a time, checking for a ready PV
-        // between chunks: a PV never waits behind a whole QK^T, so the stage
-        // it frees goes back to the producer as early as possible.
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
+        // request's epilogue).  The whole warp runs this loop in step: lane 0
+        // probes the barriers without blocking and broadcasts what it saw, and
+        // each MMA is issued by one elected lane, so operand descriptors stay
+        // warp-uniform (single-thread issue measured ~1.5x slower per MMA).
+        // QK^T goes out three 64-dim chunks (12 MMAs) per turn, with a check
+        // for a ready PV between turns: a PV never waits behind a whole QK^T.
         constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
         // Descriptors are built once; an MMA's operand then differs only in
         // the start-address field (bits 0..13, 16-byte units), which a plain
@@ -371,65 +404,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is below 256 KB).
         const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024);
         const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024);
+        const uint64_t dK1 = smem_desc(smem_u32(sKV + kStageBytes), 16, 1024);
         const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
+        const uint64_t dV1 = smem_desc(smem_u32(sKV + kStageBytes), kChunkBytes, 1024);
         const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024);
-        constexpr uint64_t kStageUnits = kStageBytes >> 4;
+        const uint32_t tS0 = tmem + kColS, tS1 = tmem + kColS + 32;
+        const uint32_t tO0 = tmem + kColO, tO1 = tmem + kColO + 128;
         constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
         Cursor qk = cursor_begin(p, part), pv = qk;
         int qk_chunk = 0;  // next 64-dim chunk of QK^T(qk.g) to issue; 0 = not started
         uint64_t idle_since = 0;
         uint32_t idle_spins = 0;
+        const bool leader = lane == 0;
         while (pv.valid) {
             bool did = false;
             if (pv.g < qk.g) {
                 const bool first = pv.blk == pv.b0;
-                bool ready = mbar_test_wait(&bars->p_full, pv.g & 1);
-                if (ready && first && pv.item > 0)
-                    ready = mbar_test_wait(&bars->o_free, (pv.item - 1) & 1);
+                bool ready = false;
+                if (leader) {
+                    ready = mbar_test_wait(&bars->p_full, pv.g & 1);
+                    if (ready && first && pv.item > 0)
+                        ready = mbar_test_wait(&bars->o_free, (pv.item - 1) & 1);
+                }
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                 if (ready) {
                     tc_fence_after();
-                    const uint64_t dV = dV0 + (pv.g & 1) * kStageUnits;
-                    const uint32_t d0 = tmem + kColO, d1 = tmem + kColO + 128;
-                    mma_ws_ss(d0, dP, dV, idesc_pv, first ? 0u : 1u);
-                    mma_ws_ss(d1, dP, dV + 4 * kChunkUnits, idesc_pv, first ? 0u : 1u);
+                    const uint64_t bV = (pv.g & 1) ? dV1 : dV0;
+                    const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-                    for (int kk = 1; kk < 4; ++kk) {
-                        mma_ws_ss(d0, dP + 2 * kk, dV + 128 * kk, idesc_pv, 1u);
-                        mma_ws_ss(d1, dP + 2 * kk, dV + 4 * kChunkUnits + 128 * kk, idesc_pv, 1u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = kk ? 1u : acc0;
+                        if (elect_one()) mma_ws_ss(tO0, dP + 2 * kk, bV + 128 * kk, idesc_pv, acc);
+                        if (elect_one())
+                            mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk, idesc_pv, acc);
                     }
-                    mma_commit(&bars->pv_done);
-                    mma_commit(&bars->kv_empty[pv.g & 1]);
+                    if (elect_one()) {
+                        mma_commit(&bars->pv_done);
+                        mma_commit(&bars->kv_empty[pv.g & 1]);
+                    }
+                    __syncwarp();
                     cursor_next(p, part, pv);
                     did = true;
                 }
             }
-            if (qk.valid) {
+            if (qk.valid && (!kStrictOrder || qk.g == pv.g)) {
                 const int st = qk.g & 1;
                 bool ready = true;
                 if (qk_chunk == 0) {
-                    if (qk.blk == qk.b0) ready = mbar_test_wait(&bars->q_full, qk.item & 1);
-                    ready = ready && mbar_test_wait(&bars->kv_full[st], (qk.g >> 1) & 1);
-                    if (ready && qk.g >= 2)
-                        ready = mbar_test_wait(&bars->s_empty[st], ((qk.g >> 1) + 1) & 1);
+                    if (leader) {
+                        if (qk.blk == qk.b0) ready = mbar_test_wait(&bars->q_full, qk.item & 1);
+                        ready = ready && mbar_test_wait(&bars->kv_full[st], (qk.g >> 1) & 1);
+                        if (ready && qk.g >= 2)
+                            ready = mbar_test_wait(&bars->s_empty[st], ((qk.g >> 1) + 1) & 1);
+                    }
+                    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                     if (ready) tc_fence_after();
                 }
                 if (ready) {
-                    // Three 64-dim chunks (12 MMAs) per turn, then look for a ready PV.
-                    const uint32_t dS = tmem + kColS + 32 * st;
-                    const uint64_t dK = dK0 + st * kStageUnits;
-                    const int c_end = qk_chunk + 3;
-                    for (int c = qk_chunk; c < c_end; ++c) {
-                        const uint64_t a = dQ + c * kChunkUnits, b = dK + c * kChunkUnits;
-                        mma_ws_ss(dS, a, b, idesc_qk, c ? 1u : 0u);
-                        mma_ws_ss(dS, a + 2, b + 2, idesc_qk, 1u);
-                        mma_ws_ss(dS, a + 4, b + 4, idesc_qk, 1u);
-                        mma_ws_ss(dS, a + 6, b + 6, idesc_qk, 1u);
-                    }
-                    qk_chunk = c_end;
+                    const uint64_t bK = st ? dK1 : dK0;
+                    const uint32_t d = st ? tS1 : tS0;
+                    if (qk_chunk == 0)
+                        issue_qk_turn<0>(dQ, bK, d);
+                    else if (qk_chunk == 3)
+                        issue_qk_turn<3>(dQ, bK, d);
+                    else
+                        issue_qk_turn<6>(dQ, bK, d);
+                    qk_chunk += 3;
                     if (qk_chunk == kChunks) {
                         qk_chunk = 0;
-                        mma_commit(&bars->s_full[st]);
-                        if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
+                        if (elect_one()) {
+                            mma_commit(&bars->s_full[st]);
+                            if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
+                        }
+                        __syncwarp();
                         cursor_next(p, part, qk);
                     }
                     did = true;
@@ -438,20 +485,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (did) {
                 idle_since = 0;
                 idle_spins = 0;
-            } else if ((++idle_spins & 63) == 0) {
-                if (*abort_flag) break;
-                const uint64_t now = globaltimer_ns();
-                if (idle_since == 0) {
-                    idle_since = now;
-                } else if (now - idle_since > p.budget_ns) {
-                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
-                    break;
+                continue;
+            }
+            // Nothing ready: back off briefly.  This warp shares its SM
+            // sub-partition with a softmax warp, and a hot polling loop would
+            // take that warp's issue slots.
+            if (kIdleSleepNs > 0) __nanosleep(kIdleSleepNs);
+            if ((++idle_spins & 63) == 0) {
+                bool stop = false;
+                if (leader) {
+                    if (*abort_flag) {
+                        stop = true;
+                    } else {
+                        const uint64_t now = globaltimer_ns();
+                        if (idle_since == 0) {
+                            idle_since = now;
+                        } else if (now - idle_since > p.budget_ns) {
+                            raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
+                            stop = true;
+                        }
+                    }
                 }
+                if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) break;
             }
         }
         // Drain: all MMAs finished before TMEM is released.
-        mma_commit(&bars->drain);
-        mbar_drain(&bars->drain, 0, kDrainBudgetNs);
+        if (elect_one()) mma_commit(&bars->drain);
+        __syncwarp();
+        if (leader) mbar_drain(&bars->drain, 0, kDrainBudgetNs);
+        __syncwarp();
     } else if (warp >= 2) {
         // ------------------------------------- softmax / correction / epilogue
         const int q4 = warp & 3;
