@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kernel", choices=["single", "pair", "rail"], default="single",
+                    help="decode kernel: single CTA (default), 2-CTA cluster pair, or two-rail")
     return ap.parse_args()
 
 
@@ -78,19 +80,23 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {"pair": ("decode_pair_kernel", "decode_attention_paged_gb300/csrc/mla_decode_pair.cu"),
+                  "single": ("decode_kernel", "decode_attention_paged_gb300/csrc/mla_decode.cu"),
+                  "rail": ("decode_rail_kernel", "decode_attention_paged_gb300/csrc/mla_decode_rail.cu")}
+
+
+def kernel_source_hash(kernel="single"):
     h = hashlib.sha256()
-    for rel in ("decode_attention_paged_gb300/csrc/mla_decode.cu",
-                "decode_attention_paged_gb300/csrc/sm103_ptx.cuh"):
+    for rel in (KERNEL_SOURCES[kernel][1], "decode_attention_paged_gb300/csrc/sm103_ptx.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profile_traffic(workload):
+def profile_traffic(workload, kernel="single"):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}_ncu.txt")
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_SOURCES[kernel][0]}_{workload}_ncu.txt")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -99,7 +105,7 @@ def profile_traffic(workload):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if vals.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -422,6 +428,8 @@ def main():
     from decode_attention_paged_gb300 import api
     from decode_attention_paged_gb300 import workloads as W_mod
 
+    api.set_decode_kernel({"single": api.KERNEL_SINGLE, "pair": api.KERNEL_PAIR,
+                           "rail": api.KERNEL_RAIL}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     # weak scaling: every rank decodes its own batch of requests (replicas).
     w = W_mod.CONFIGS[args.workload](seed_offset=1000 * rank)
@@ -456,10 +464,10 @@ def main():
     clocks = sampler.summary() if sampler else None
     dec_ms = res["ms_decode"]
     achieved = res["bytes"] / (dec_ms * 1e-3) / 1e9
-    traffic = profile_traffic(args.workload)
+    traffic = profile_traffic(args.workload, args.kernel)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": "decode_kernel (split-KV)", "peak_source": peak_src,
+                "kernel": KERNEL_SOURCES[args.kernel][0] + " (split-KV)", "peak_source": peak_src,
                 "tensor_frac_of_bf16_peak": res["flops"] / (dec_ms * 1e-3) / 1e12 / bf16_peak,
                 "ms_per_launch": dec_ms, "launches_timed": res["kernel_steps"]}
 

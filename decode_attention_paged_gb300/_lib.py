@@ -46,6 +46,8 @@ SIGNATURES = {
     "mla_last_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "mla_set_wait_budget_ns": (_I, [ctypes.c_uint64]),
     "mla_set_fixed_overhead": (_I, [_I]),
+    "mla_set_decode_kernel": (_I, [_I]),
+    "mla_get_decode_kernel": (_I, []),
 }
 
 _lib = None

@@ -179,6 +179,20 @@ def set_fixed_overhead(blocks: int) -> None:
     _lib.check(_lib.load().mla_set_fixed_overhead(int(blocks)), "mla_set_fixed_overhead")
 
 
+KERNEL_PAIR = 0    # one 2-CTA cluster per SM pair, head dims split across the pair
+KERNEL_SINGLE = 1  # one CTA per SM holding all 576 dims (default)
+KERNEL_RAIL = 2    # one CTA per SM, Q in tensor memory, two-rail QK^T
+
+
+def set_decode_kernel(kind: int) -> None:
+    """Select the decode kernel (process-wide); rebuild metadata afterwards."""
+    _lib.check(_lib.load().mla_set_decode_kernel(int(kind)), "mla_set_decode_kernel")
+
+
+def get_decode_kernel() -> int:
+    return int(_lib.load().mla_get_decode_kernel())
+
+
 def flash_mla_with_kvcache(q, k_cache, block_table, cache_seqlens, head_dim_v, meta, num_splits,
                            softmax_scale=None, causal=False):
     """The pages' call shape (flash_mla_with_kvcache) mapped onto mla_decode_fwd."""

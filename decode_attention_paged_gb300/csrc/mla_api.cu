@@ -25,10 +25,12 @@ constexpr int kDefaultFixedOverhead = 2;
 
 std::atomic<uint64_t> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_fixed_overhead{kDefaultFixedOverhead};
+std::atomic<int> g_kernel{MLA_KERNEL_SINGLE};
 
 struct DeviceInfo {
     std::once_flag once;
     int sms = 0;
+    int pair_clusters = 0;  // co-resident 2-CTA clusters of the pair kernel
     int major = 0, minor = 0;
     int* error_word = nullptr;
     cudaError_t status = cudaSuccess;
@@ -57,6 +59,10 @@ int device_info(DeviceInfo** out) {
             d.status = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (d.status == cudaSuccess)
             d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), g_mla_error_word);
+        if (d.status == cudaSuccess && d.major == 10 && d.minor == 3) {
+            d.pair_clusters = pair_max_active_clusters();
+            if (d.pair_clusters <= 0) d.pair_clusters = d.sms / 2;
+        }
     });
     if (d.status != cudaSuccess) return MLA_ERR_CUDA;
     // The kernels are built for sm_103a only.
@@ -67,9 +73,13 @@ int device_info(DeviceInfo** out) {
 
 int n_mtiles_of(int R) { return (R + kTileM - 1) / kTileM; }
 
-int num_parts_of(int R, int sms) {
+// SM parts of the split plan: as many (part, query tile) work units as the
+// selected kernel keeps resident at once -- one CTA per SM for the single-CTA
+// kernel, one 2-CTA cluster per SM pair for the pair kernel.
+int num_parts_of(int R, const DeviceInfo* d) {
     const int mt = n_mtiles_of(R);
-    const int parts = sms / mt;
+    const int units = g_kernel.load() == MLA_KERNEL_PAIR ? d->pair_clusters : d->sms;
+    const int parts = units / mt;
     return parts > 0 ? parts : 1;
 }
 
@@ -144,6 +154,15 @@ int mla_set_wait_budget_ns(uint64_t budget_ns) {
     return MLA_OK;
 }
 
+int mla_set_decode_kernel(int kind) {
+    if (kind != MLA_KERNEL_PAIR && kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_RAIL)
+        return MLA_ERR_INVALID_ARGUMENT;
+    g_kernel.store(kind);
+    return MLA_OK;
+}
+
+int mla_get_decode_kernel(void) { return g_kernel.load(); }
+
 int mla_set_fixed_overhead(int blocks) {
     g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead : (blocks < 1 ? 1 : blocks));
     return MLA_OK;
@@ -155,7 +174,7 @@ int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
     if (st) return st;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int parts = num_parts_of(s_q * h_q, d->sms);
+    const int parts = num_parts_of(s_q * h_q, d);
     if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
     if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(batch) + 1);
     return MLA_OK;
@@ -172,7 +191,7 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
-    const int parts = num_parts_of(R, d->sms);
+    const int parts = num_parts_of(R, d);
     cudaError_t e = launch_sched(cache_seqlens_dev, batch, R, parts, n_mtiles_of(R),
                                  g_fixed_overhead.load(), static_cast<int32_t*>(meta_dev),
                                  num_splits_dev, reinterpret_cast<cudaStream_t>(stream));
@@ -187,7 +206,7 @@ int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
     size_t ob = 0;
-    workspace_layout(batch, R, num_parts_of(R, d->sms), &ob, bytes);
+    workspace_layout(batch, R, num_parts_of(R, d), &ob, bytes);
     return MLA_OK;
 }
 
@@ -212,7 +231,7 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
     size_t o_bytes = 0, ws_need = 0;
-    workspace_layout(batch, R, num_parts_of(R, d->sms), &o_bytes, &ws_need);
+    workspace_layout(batch, R, num_parts_of(R, d), &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
     CombineParams c{};
@@ -262,7 +281,7 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
-    const int parts = num_parts_of(R, d->sms);
+    const int parts = num_parts_of(R, d);
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(batch, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -304,7 +323,11 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.error_word = d->error_word;
     p.budget_ns = g_budget_ns.load();
 
-    cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int kind = g_kernel.load();
+    cudaError_t e = kind == MLA_KERNEL_PAIR   ? launch_decode_pair(p, q_map, kv_map, s)
+                    : kind == MLA_KERNEL_RAIL ? launch_decode_rail(p, q_map, kv_map, s)
+                                              : launch_decode(p, q_map, kv_map, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -1,0 +1,794 @@
+// mla_decode_rail.cu -- split-KV paged MLA decode for sm_103a with the query
+// tile in tensor memory and QK^T as a two-rail weight-stationary GEMM.
+//
+// Sources (web pages, cited by title and section):
+//   [Overview] "[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐":
+//       sec. 3 (one 576-dim cache row is K; its first 512 dims are V),
+//       sec. 4 (paged KV through block_table), sec. 6 (split-KV partials),
+//       sec. 7 (online softmax makes the partials mergeable).
+//   [Rails] "Blackwell 多轨矩乘(multi-rail GEMM):FlashMLA 如何用一条 MMA 算完两路
+//       QK", sec. 1.2 (M=64 .ws: lane group g multiplies its own A rows by
+//       the g-th half of B's N), sec. 2.1-2.3 (store different feature dims
+//       of Q in the two lane groups, reinterpret one KV tile as 2T rows of
+//       half the dims, add the two partial score tiles after masking),
+//       sec. 3.2 (the saving is tensor memory, not multiplications).
+//   [DeepDive] "FlashMLA 新内核深度解析：Seesaw 调度、细粒度 TMA 流水线与 H800
+//       上的 660 TFlops MLA 解码": "细粒度 TMA copy-GEMM 流水线" (a 64x576 K
+//       tile moves as 64x64 TMA copies), "缓存提示" (EVICT_FIRST), the exp ->
+//       exp2 rewrite (end of the Seesaw section), "Programmatic Dependent
+//       Launch", "Tile Scheduler" (each SM part walks its DecodingSchedMeta).
+//   [AttnBook] "3.4 Attention kernel": "在线 softmax", 代码 (causal mask).
+//
+// Why this shape.  A 64 x 576 bf16 Q tile held in shared memory (72 KB) next
+// to 72 KB KV pages leaves room for two pages in flight, and on sm_103a the
+// per-SM bandwidth share needs more: every page waits out an HBM round trip
+// plus QK^T -> softmax -> PV before its buffer is refilled.  Here Q lives in
+// tensor memory as the A operand of QK^T, so shared memory holds three pages
+// (two when the query tile has more than 32 rows and the rail exchange needs a
+// buffer of its own).  Q in tensor memory would need 288 columns per lane
+// group as the replicated operand of a plain weight-stationary MMA -- with the
+// 256 columns of O that is more than the 512 there are -- so the two lane
+// groups hold different dims of Q (two rails):
+//   k-step j = 4 p + kk (p < 4): rail 0 = dims of chunk 2p, rail 1 = chunk 2p+1
+//   k-step 16 + kk:              rail 0 = zero, rail 1 = the RoPE chunk 8
+// with the 16 dims [16 kk, 16 kk + 16) of the chunk each.  One MMA with N =
+// 128 reads B rows 0..63 from chunk c and rows 64..127 from chunk c + 1 of
+// the same page (chunks are 8 KB apart), so every KV page is read once, as
+// stored; the RoPE steps use chunk 7 as rail 0's partner, multiplied by the
+// zero rail-0 Q.  Lane group g ends with the partial scores of rail g for
+// all 64 tokens; the two partials of a row are added by the softmax threads
+// after a swap through shared memory (for tiles of at most 32 rows the swap
+// uses the page's RoPE chunk, dead once QK^T is done), rail 0 first, and a
+// masked token takes -inf before any addition.
+//
+// Tensor memory (512 columns): O [64 x 512] fp32 as two weight-stationary
+// N=256 halves at columns 0 and 128 (lanes 0..63 dims 256h + [0,128), lanes
+// 64..127 dims 256h + [128,256)); Q rails at 256..415 (20 k-steps x 8
+// columns, bf16 pairs); S partials at 416..479 (64 columns per lane group).
+//
+// The query tile arrives through the KV ring as a pseudo page (the producer
+// puts each request's Q tile in the ring ahead of its pages); the softmax
+// threads move their rows from the swizzled stage into their TMEM lanes.
+//
+// Warp roles (warp w runs on SM sub-partition w % 4 and reaches TMEM lanes
+// 32 (w % 4) .. + 31): warps 0..3 softmax / rail swap / correction / epilogue
+// (one thread per TMEM lane; for tiles of at most 32 valid rows only warps 0
+// and 2 take part), warp 4 TMA producer (one thread), warp 5 TMEM owner and
+// QK^T issuer, warp 7 PV issuer (elect.sync issue from converged warps).
+//
+// Every wait is bounded; a timeout records MLA_ERR_DEVICE_TIMEOUT, drains the
+// CTA's own copies and MMAs, frees TMEM and returns.
+#include "mla_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+#ifndef MLA_RAIL_PRODUCER_WARP
+#define MLA_RAIL_PRODUCER_WARP 4
+#endif
+#ifndef MLA_RAIL_QK_WARP
+#define MLA_RAIL_QK_WARP 5
+#endif
+#ifndef MLA_RAIL_PV_WARP
+#define MLA_RAIL_PV_WARP 7
+#endif
+constexpr int kProducerWarp = MLA_RAIL_PRODUCER_WARP;
+constexpr int kQkWarp = MLA_RAIL_QK_WARP;
+constexpr int kPvWarp = MLA_RAIL_PV_WARP;
+constexpr int kMaxRoleWarp =
+    kProducerWarp > kQkWarp ? (kProducerWarp > kPvWarp ? kProducerWarp : kPvWarp)
+                            : (kQkWarp > kPvWarp ? kQkWarp : kPvWarp);
+constexpr int kThreads = 32 * (kMaxRoleWarp + 1);
+static_assert(kProducerWarp >= 4 && kQkWarp >= 4 && kPvWarp >= 4 && kProducerWarp != kQkWarp &&
+                  kProducerWarp != kPvWarp && kQkWarp != kPvWarp,
+              "warp roles overlap the softmax warps or each other");
+
+constexpr int kMaxStages = 3;
+constexpr uint32_t kStageBytes = kChunks * kChunkBytes;  // 73728
+constexpr uint32_t kPBytes = 64 * 128;                   // P [64 rows x 64 tokens] bf16
+constexpr uint32_t kSmemMax = 232448;                    // 227 KB per CTA
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;    // two PV halves of 128 columns
+constexpr uint32_t kColQ = 256;  // 20 k-steps x 8 columns
+constexpr uint32_t kColS = 416;  // 64 columns per lane group
+constexpr int kQkSteps = 20;
+constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
+constexpr uint64_t kDrainBudgetNs = 2000000000ull;
+constexpr uint32_t kReadAhead = 8;  // block-table entries read ahead
+constexpr int kPageRing = 16;
+
+struct Barriers {
+    uint64_t kv_full[kMaxStages];
+    uint64_t kv_empty[kMaxStages];
+    uint64_t q_ready;  // this request's Q rails are in TMEM
+    uint64_t s_full, s_empty;
+    uint64_t p_full, pv_done;
+    uint64_t o_free;
+    uint64_t drain_qk, drain_pv;
+};
+static_assert(sizeof(Barriers) <= 256, "barrier block");
+
+// Shared-memory layout as a function of the rows one Q tile load brings.
+struct RailLayout {
+    uint32_t n_stages;
+    bool x_in_stage;  // rail swap through the page's RoPE chunk
+    uint32_t off_p, off_x, off_m, off_bar, off_misc, bytes;
+};
+__host__ __device__ constexpr RailLayout rail_layout(int q_box_rows) {
+    RailLayout l{};
+    l.x_in_stage = q_box_rows <= 32;
+    l.n_stages = l.x_in_stage ? 3u : 2u;
+    l.off_p = l.n_stages * kStageBytes;
+    l.off_x = l.off_p + kPBytes;
+    l.off_m = l.off_x + (l.x_in_stage ? 0u : 128u * 128u);  // 128 slots x 128 bytes
+    l.off_bar = l.off_m + 2560u;  // tagged swaps: uint2 v[2][128], then uint32 x tags[128]
+    l.off_misc = l.off_bar + 256u;                           // tmem base, abort flag
+    l.bytes = l.off_misc + 64u;
+    return l;
+}
+static_assert(rail_layout(16).bytes <= kSmemMax && rail_layout(32).bytes <= kSmemMax &&
+                  rail_layout(64).bytes <= kSmemMax,
+              "exceeds the 227 KB per-CTA shared memory limit");
+static_assert(kSmemMax < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
+
+struct Part {
+    int begin_req, end_req, begin_block, end_block, begin_split;
+};
+
+__device__ __forceinline__ int blocks_of(int L) { return L > 0 ? (L + kPage - 1) / kPage : 0; }
+
+__device__ __forceinline__ void item_range(const DecodeParams& p, const Part& part, int req,
+                                           int& L, int& nb, int& b0, int& b1) {
+    L = p.seqlens[req];
+    if (L < 0) L = 0;
+    nb = blocks_of(L);
+    if (nb > p.max_blocks) nb = p.max_blocks;  // reported as MLA_ERR_SEQ_TOO_LONG
+    if (L > nb * kPage) L = nb * kPage;
+    b0 = (req == part.begin_req) ? part.begin_block : 0;
+    b1 = (req == part.end_req) ? part.end_block : nb;
+    if (b1 > nb) b1 = nb;
+    if (b0 < 0) b0 = 0;
+    if (b0 > b1) b0 = b1;
+}
+
+// Walk over the non-empty (request, block) pairs of a part.  g counts pages,
+// item counts requests with at least one block; the ring holds each such
+// request's Q tile followed by its pages, so page g of item i sits at ring
+// index g + i + 1 and the item's Q tile at g_first + i.
+struct Cursor {
+    int req, blk, b0, b1, L, nb;
+    uint32_t g;
+    uint32_t item;
+    bool valid;
+    __device__ __forceinline__ uint32_t ring() const { return g + item + 1; }
+};
+__device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& part, Cursor& c,
+                                            int req) {
+    for (; req <= part.end_req; ++req) {
+        item_range(p, part, req, c.L, c.nb, c.b0, c.b1);
+        if (c.b1 > c.b0) {
+            c.req = req;
+            c.blk = c.b0;
+            c.valid = true;
+            return;
+        }
+    }
+    c.valid = false;
+}
+__device__ __forceinline__ Cursor cursor_begin(const DecodeParams& p, const Part& part) {
+    Cursor c;
+    c.g = 0;
+    c.item = 0;
+    cursor_seek(p, part, c, part.begin_req);
+    return c;
+}
+__device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& part, Cursor& c) {
+    ++c.g;
+    if (++c.blk < c.b1) return;
+    ++c.item;
+    cursor_seek(p, part, c, c.req + 1);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, wc, MLA_ERR_DEVICE_TIMEOUT);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        __threadfence_block();
+        mbar_arrive(bar);
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
+                                             uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Bounded spin until the partner's tag reaches `want`; warp-uniform verdict.
+__device__ __forceinline__ bool wait_tag(uint32_t tag_addr, uint32_t want, const WaitCtx& wc) {
+    bool ok = true;
+    uint32_t got;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(got) : "r"(tag_addr) : "memory");
+    if (got != want) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+            asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(got) : "r"(tag_addr) : "memory");
+            if (got == want) break;
+            if ((spin & 255) == 0) {
+                if (*wc.abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > wc.budget_ns) {
+                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    __threadfence_block();
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Swap one float with the thread holding the other rail of the same row
+// (TMEM lane L <-> L ^ 64): value and tag go out in one 8-byte store, into
+// one of two slot sets chosen by the tag's parity, so that a slot is rewritten
+// only after the partner has answered the swap that read it.
+__device__ __forceinline__ bool swap_value(uint2* slot_sets, int lrow, uint32_t& seq, float v,
+                                           float& partner, const WaitCtx& wc) {
+    const uint32_t tag = ++seq;
+    uint2* slots = slot_sets + (tag & 1) * 128;
+    asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(slots + lrow)),
+                 "r"(__float_as_uint(v)), "r"(tag)
+                 : "memory");
+    const uint32_t src = smem_u32(slots + (lrow ^ 64));
+    bool ok = true;
+    uint2 got;
+    asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(got.x), "=r"(got.y) : "r"(src)
+                 : "memory");
+    if (got.y != tag) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+            asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(got.x), "=r"(got.y)
+                         : "r"(src)
+                         : "memory");
+            if (got.y == tag) break;
+            if ((spin & 255) == 0) {
+                if (*wc.abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > wc.budget_ns) {
+                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+    }
+    partner = __uint_as_float(got.x);
+    return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_rail_kernel(const __grid_constant__ DecodeParams p,
+                       const __grid_constant__ CUtensorMap q_map,
+                       const __grid_constant__ CUtensorMap kv_map) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int mtile = blockIdx.x, part_idx = blockIdx.y;
+    const RailLayout lay = rail_layout(p.q_box_rows);
+    const uint32_t n_stages = lay.n_stages;
+    int rows_valid = p.R - mtile * kTileM;
+    rows_valid = rows_valid > kTileM ? kTileM : rows_valid;
+    // Softmax warps 1 and 3 hold rows 32..63 only; they sit out when those
+    // rows do not exist.
+    const uint32_t n_active = rows_valid > 32 ? 4u : 2u;
+    const bool softmax_warp = warp < 4 && (n_active == 4 || (warp & 1) == 0);
+
+    uint8_t* sKV = smem;
+    uint8_t* sP = smem + lay.off_p;
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + lay.off_bar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.off_misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.off_misc + 4);
+    WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
+
+    // ------------------------------------------------------------ prologue
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (uint32_t s = 0; s < n_stages; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        mbar_init(&bars->q_ready, n_active);
+        mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_empty, n_active);
+        mbar_init(&bars->p_full, n_active);
+        mbar_init(&bars->pv_done, 1);
+        mbar_init(&bars->o_free, n_active);
+        mbar_init(&bars->drain_qk, 1);
+        mbar_init(&bars->drain_pv, 1);
+        fence_barrier_init();
+        uint32_t* tags = reinterpret_cast<uint32_t*>(smem + lay.off_m);
+        for (int i = 0; i < 2560 / 4; ++i) tags[i] = 0u;
+        prefetch_tensormap(&q_map);
+        prefetch_tensormap(&kv_map);
+    }
+    if (warp == kQkWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_wait_primary();
+
+    bool ok = (smem_u32(smem) & 1023u) == 0;
+    const int32_t* hdr = p.meta;
+    if (ok && (hdr[kHMagic] != kMetaMagic || hdr[kHBatch] != p.batch || hdr[kHRows] != p.R ||
+               hdr[kHParts] != p.num_parts || hdr[kHMTiles] != p.n_mtiles ||
+               hdr[kHPage] != kPage))
+        ok = false;
+    Part part{};
+    if (ok) {
+        const int32_t* rec = hdr + kMetaHeader + part_idx * kMetaFields;
+        part.begin_req = rec[kBeginReq];
+        part.end_req = rec[kEndReq];
+        part.begin_block = rec[kBeginBlock];
+        part.end_block = rec[kEndBlock];
+        part.begin_split = rec[kBeginSplit];
+        if (part.begin_req < p.batch &&
+            (part.begin_req < 0 || part.end_req >= p.batch || part.end_req < part.begin_req))
+            ok = false;
+        if (part.begin_req >= p.batch) part.end_req = part.begin_req - 1;
+    }
+    if (!ok) {
+        if (tid == 0) raise_error(wc, MLA_ERR_METADATA_MISMATCH);
+        part.begin_req = 0;
+        part.end_req = -1;
+    }
+    if (tid == 0) {
+        for (int req = part.begin_req; req <= part.end_req; ++req) {
+            const int L = p.seqlens[req];
+            if (L > 0 && blocks_of(L) > p.max_blocks) raise_error(wc, MLA_ERR_SEQ_TOO_LONG);
+        }
+    }
+
+    if (warp == kProducerWarp && lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        const uint64_t policy = policy_evict_first();
+        const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
+        Cursor ld = cursor_begin(p, part), pf = ld;
+        int ring[kPageRing];
+        uint32_t n_issued = 0;  // ring entries issued
+        while (ld.valid) {
+            while (pf.valid && pf.g <= ld.g + kReadAhead) {
+                ring[pf.g % kPageRing] =
+                    p.block_table[static_cast<int64_t>(pf.req) * p.bt_stride + pf.blk];
+                cursor_next(p, part, pf);
+            }
+            bool stop = false;
+            // First block of a request: its Q tile goes into the ring first.
+            for (int entry = (ld.blk == ld.b0) ? 0 : 1; entry < 2; ++entry) {
+                const uint32_t n = ld.ring() - 1 + entry;
+                const uint32_t st = n % n_stages;
+                if (n >= n_stages &&
+                    !mbar_wait(&bars->kv_empty[st], ((n / n_stages) + 1) & 1, wc,
+                               MLA_ERR_DEVICE_TIMEOUT)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t* dst = sKV + st * kStageBytes;
+                if (entry == 0) {
+                    mbar_arrive_expect_tx(&bars->kv_full[st], q_bytes);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(&q_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
+                                    mtile * kTileM, ld.req, policy);
+                } else {
+                    const int page = ring[ld.g % kPageRing];
+                    mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0,
+                                    page, policy);
+                }
+                n_issued = n + 1;
+            }
+            if (stop) break;
+            cursor_next(p, part, ld);
+        }
+        for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k)
+            mbar_drain(&bars->kv_full[k % n_stages], (k / n_stages) & 1, kDrainBudgetNs);
+    } else if (warp == kQkWarp) {
+        // ------------------------------------------------------ QK^T issuer
+        // Page g needs its stage, its request's Q rails and a free S buffer.
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 128, false, false);
+        const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024);
+        constexpr uint64_t kStageUnits = kStageBytes >> 4;
+        constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
+        const uint32_t tS = tmem + kColS, tQ = tmem + kColQ;
+        for (Cursor qk = cursor_begin(p, part); qk.valid; cursor_next(p, part, qk)) {
+            const uint32_t n = qk.ring();
+            const uint32_t st = n % n_stages;
+            if (qk.blk == qk.b0) {
+                // The softmax warps copied this request's Q tile into the
+                // rails; its ring stage (the entry before this page) is free.
+                if (!warp_wait(&bars->q_ready, qk.item & 1, wc)) break;
+                if (lane == 0) mbar_arrive(&bars->kv_empty[(n - 1) % n_stages]);
+            }
+            if (!warp_wait(&bars->kv_full[st], (n / n_stages) & 1, wc)) break;
+            if (qk.g >= 1 && !warp_wait(&bars->s_empty, (qk.g - 1) & 1, wc)) break;
+            tc_fence_after();
+            const uint64_t bK = dK0 + st * kStageUnits;
+#pragma unroll
+            for (int j = 0; j < kQkSteps; ++j) {
+                const int pair = j < 16 ? j / 4 : 0;
+                const int kk = j & 3;
+                // rail 0 chunk (rail 1 reads the chunk 8 KB after it)
+                const uint64_t chunk = j < 16 ? 2 * pair : 7;
+                if (elect_one())
+                    mma_ws_ts(tS, tQ + 8 * j, bK + chunk * kChunkUnits + 2 * kk, idesc_qk,
+                              j ? 1u : 0u);
+            }
+            if (elect_one()) mma_commit(&bars->s_full);
+            __syncwarp();
+        }
+        if (elect_one()) mma_commit(&bars->drain_qk);
+        __syncwarp();
+        if (lane == 0) mbar_drain(&bars->drain_qk, 0, kDrainBudgetNs);
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------ PV issuer
+        // Page g needs P(g) and, on a request's first block, O released by
+        // the previous request's epilogue.
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
+        const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
+        const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024);
+        constexpr uint64_t kStageUnits = kStageBytes >> 4;
+        constexpr uint64_t kHalfUnits = (4 * kChunkBytes) >> 4;
+        for (Cursor pv = cursor_begin(p, part); pv.valid; cursor_next(p, part, pv)) {
+            const bool first = pv.blk == pv.b0;
+            const uint32_t st = pv.ring() % n_stages;
+            if (!warp_wait(&bars->p_full, pv.g & 1, wc)) break;
+            if (first && pv.item > 0 && !warp_wait(&bars->o_free, (pv.item - 1) & 1, wc)) break;
+            tc_fence_after();
+            const uint64_t bV = dV0 + st * kStageUnits;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    if (elect_one())
+                        mma_ws_ss(tmem + kColO + 128 * h, dP + 2 * kk,
+                                  bV + h * kHalfUnits + 128 * kk, idesc_pv,
+                                  (first && kk == 0) ? 0u : 1u);
+            if (elect_one()) {
+                mma_commit(&bars->pv_done);
+                mma_commit(&bars->kv_empty[st]);
+            }
+            __syncwarp();
+        }
+        if (elect_one()) mma_commit(&bars->drain_pv);
+        __syncwarp();
+        if (lane == 0) mbar_drain(&bars->drain_pv, 0, kDrainBudgetNs);
+        __syncwarp();
+    } else if (softmax_warp) {
+        // -------------- rail swap / softmax / correction / epilogue / Q copy
+        const int q4 = warp;              // TMEM lane quadrant
+        const int Lrow = 32 * q4 + lane;  // TMEM lane
+        const int r = Lrow & 63, grp = Lrow >> 6;
+        const int row = mtile * kTileM + r;
+        const bool row_valid = r < rows_valid;
+        const int s_idx = row / p.h_q, h_idx = row % p.h_q;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        const int me = n_active == 4 ? tid : (32 * (warp >> 1) + lane);  // among active threads
+        // Rail swap slots (128 bytes each, 16-byte units rotated by lane).
+        const int x_slot = lay.x_in_stage ? (lane + 32 * grp) : Lrow;
+        const int x_peer = lay.x_in_stage ? (lane + 32 * (grp ^ 1)) : (Lrow ^ 64);
+        uint2* v_swap = reinterpret_cast<uint2*>(smem + lay.off_m);  // [2][128] value + tag
+        const uint32_t x_tag_own = smem_u32(smem + lay.off_m + 2048 + Lrow * 4);
+        const uint32_t x_tag_peer = smem_u32(smem + lay.off_m + 2048 + (Lrow ^ 64) * 4);
+        uint32_t vseq = 0, xseq = 0;
+        uint32_t gblk = 0, item = 0;
+        bool alive = true;
+        for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
+            int L, nb, b0, b1;
+            item_range(p, part, req, L, nb, b0, b1);
+            int lim = L;
+            if (p.causal) {
+                lim = L - p.s_q + s_idx + 1;
+                lim = lim < 0 ? 0 : (lim > L ? L : lim);
+            }
+            const int first_piece = p.num_splits[req];
+            const bool split = (p.num_splits[req + 1] - first_piece) > 1;
+            const int slot = (req == part.begin_req) ? part.begin_split : first_piece;
+            const bool has_blocks = b1 > b0;
+            if (has_blocks) {
+                // Q tile of this request: from its ring stage into the rails.
+                const uint32_t nq = gblk + item;
+                const uint32_t stq = nq % n_stages;
+                if (!warp_wait(&bars->kv_full[stq], (nq / n_stages) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                const uint8_t* sq = sKV + stq * kStageBytes;
+                const bool have = r < p.q_box_rows;
+#pragma unroll 1
+                for (int k = 0; k < 5; ++k) {
+                    const int c = grp == 0 ? 2 * k : (k < 4 ? 2 * k + 1 : 8);
+                    uint32_t w[32];
+                    if (have && !(grp == 0 && k == 4)) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            ld_shared_v4(smem_u32(sq + c * kChunkBytes + sw128_offset(r, u)),
+                                         w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = 0u;
+                    }
+                    tmem_st32(tl + kColQ + 32 * k, w);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(&bars->q_ready);
+            }
+            float m_used = -INFINITY, l_part = 0.f;
+            for (int blk = b0; blk < b1; ++blk, ++gblk) {
+                const uint32_t n = gblk + item + 1;
+                const uint32_t st = n % n_stages;
+                uint8_t* stage = sKV + st * kStageBytes;
+                if (!warp_wait(&bars->s_full, gblk & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t own[64];
+                tmem_ld32(tl + kColS, *reinterpret_cast<uint32_t(*)[32]>(own));
+                tmem_ld32(tl + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
+                tmem_ld_wait();
+                tc_fence_before();
+                warp_arrive(&bars->s_empty);
+
+                // Swap rail partials with the thread holding the other rail of
+                // this row: rail 0 keeps tokens 0..31, rail 1 tokens 32..63.
+                const uint32_t x_base =
+                    lay.x_in_stage ? smem_u32(stage + 8 * kChunkBytes) : smem_u32(smem + lay.off_x);
+                const uint32_t send = x_base + x_slot * 128, recv = x_base + x_peer * 128;
+                // the tokens the partner keeps: rail 0 gives 32..63, rail 1 gives 0..31
+                const bool g0 = grp == 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t u = (k ^ (lane & 7)) * 16;
+                    st_shared_v4(send + u, g0 ? own[32 + 4 * k] : own[4 * k],
+                                 g0 ? own[33 + 4 * k] : own[4 * k + 1],
+                                 g0 ? own[34 + 4 * k] : own[4 * k + 2],
+                                 g0 ? own[35 + 4 * k] : own[4 * k + 3]);
+                }
+                __threadfence_block();
+                asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(x_tag_own), "r"(++xseq)
+                             : "memory");
+                if (!wait_tag(x_tag_peer, xseq, wc)) {
+                    alive = false;
+                    break;
+                }
+                uint32_t other[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t u = (k ^ (lane & 7)) * 16;
+                    ld_shared_v4(recv + u, other[4 * k], other[4 * k + 1], other[4 * k + 2],
+                                 other[4 * k + 3]);
+                }
+                const int keep = grp == 0 ? 0 : 32;
+                const int t0 = blk * kPage + keep;
+                float x[32];
+                float hmax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float r0 = __uint_as_float(grp == 0 ? own[c] : other[c]);
+                    const float r1 = __uint_as_float(grp == 0 ? other[c] : own[32 + c]);
+                    x[c] = (row_valid && t0 + c < lim) ? (r0 + r1) * p.scale_log2 : -INFINITY;
+                    hmax = fmaxf(hmax, x[c]);
+                }
+                float pmax;
+                if (!swap_value(v_swap, Lrow, vseq, hmax, pmax, wc)) {
+                    alive = false;
+                    break;
+                }
+                const float tmax = fmaxf(hmax, pmax);
+                float alpha = 1.f;
+                bool need = false;
+                if (tmax > m_used + kLazyThreshold) {
+                    alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - tmax);
+                    m_used = tmax;
+                    need = true;
+                }
+                if (need) l_part *= alpha;
+                uint32_t pk[16];
+                float psum = 0.f;
+                const bool none = (m_used == -INFINITY);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = none ? 0.f : fast_exp2(x[2 * c] - m_used);
+                    const float p1 = none ? 0.f : fast_exp2(x[2 * c + 1] - m_used);
+                    psum += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                l_part += psum;
+
+                // P and O are single buffers: PV(g - 1) must be done.
+                if (gblk > 0 && !warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need && blk > b0)) {
+                    const float a = (need && blk > b0) ? alpha : 1.f;
+#pragma unroll 1
+                    for (int cg = 0; cg < 8; ++cg) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + kColO + 32 * cg, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+                        tmem_st32(tl + kColO + 32 * cg, o);
+                    }
+                    tmem_st_wait();
+                }
+                // Last page of the sequence: zero the V rows past its length
+                // (they may hold any bits, and 0 * NaN would poison the sum).
+                if (blk == nb - 1 && (L & (kPage - 1)) != 0) {
+                    const int tail0 = L & (kPage - 1);
+                    const int per_chunk = (kPage - tail0) * 8;
+                    for (int i = me; i < 8 * per_chunk; i += 32 * static_cast<int>(n_active)) {
+                        const int c = i / per_chunk, u = i % per_chunk;
+                        reinterpret_cast<uint4*>(stage + c * kChunkBytes + tail0 * 128)[u] =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = sw128_offset(r, 4 * grp + k);
+                    *reinterpret_cast<uint4*>(sP + off) =
+                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                warp_arrive(&bars->p_full);
+            }
+            if (!alive) break;
+
+            // ---------------------------------------------------- epilogue
+            float l_tot = 0.f;
+            if (has_blocks) {
+                if (!warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                float l_other;
+                if (!swap_value(v_swap, Lrow, vseq, l_part, l_other, wc)) {
+                    alive = false;
+                    break;
+                }
+                l_tot = l_part + l_other;
+            }
+            const bool empty = !(l_tot > 0.f);
+            const float inv = empty ? 0.f : 1.f / l_tot;
+            const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
+            const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
+            if (has_blocks) {
+#pragma unroll 1
+                for (int cg = 0; cg < 8; ++cg) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + kColO + 32 * cg, o);
+                    tmem_ld_wait();
+                    const int dv0 = 256 * (cg >> 2) + 128 * grp + 32 * (cg & 3);
+                    if (!row_valid) continue;
+                    if (split) {
+                        float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv,
+                                                 __uint_as_float(o[4 * v + 1]) * inv,
+                                                 __uint_as_float(o[4 * v + 2]) * inv,
+                                                 __uint_as_float(o[4 * v + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            p.out + req * p.out_sb + s_idx * p.out_ss + h_idx * p.out_sh + dv0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                w[j] = pack_bf16x2(__uint_as_float(o[8 * v + 2 * j]) * inv,
+                                                   __uint_as_float(o[8 * v + 2 * j + 1]) * inv);
+                            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                warp_arrive(&bars->o_free);
+                ++item;
+            } else if (row_valid) {
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int dv0 = 256 * hh + 128 * grp;
+                    if (split) {
+                        float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
+                        for (int v = 0; v < 32; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            p.out + req * p.out_sb + s_idx * p.out_ss + h_idx * p.out_sh + dv0);
+                        for (int v = 0; v < 16; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            if (row_valid && grp == 0) {
+                if (split)
+                    p.lseaccum[acc_row] = lse2;
+                else
+                    p.lse[(static_cast<int64_t>(req) * p.h_q + h_idx) * p.s_q + s_idx] =
+                        empty ? -INFINITY : lse2 * 0.69314718055994531f;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+static cudaError_t rail_set_smem() {
+    static int configured_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 31 || !(__atomic_load_n(&configured_mask, __ATOMIC_RELAXED) & (1 << dev))) {
+        e = cudaFuncSetAttribute(decode_rail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemMax));
+        if (e != cudaSuccess) return e;
+        if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_rail(const DecodeParams& p, const CUtensorMap& q_map,
+                               const CUtensorMap& kv_map, cudaStream_t stream) {
+    cudaError_t e = rail_set_smem();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_mtiles, p.num_parts, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = rail_layout(p.q_box_rows).bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_rail_kernel, p, q_map, kv_map);
+}
+
+}  // namespace mla

@@ -1,0 +1,87 @@
+"""Both decode kernels (the 2-CTA cluster pair that splits the head dims, and the
+single-CTA one) against the fp64 oracle on the same seeded cases, and the
+metadata check that catches a plan built for the other kernel.
+Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_attention_paged_gb300 import _lib
+from decode_attention_paged_gb300 import workloads as W
+from tests._helpers import NTHREADS, assert_close, problem, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # (b, s_q, h_q, seqlens, causal): tails, splits, causal rows that see
+    # nothing, several query tiles, an empty request
+    (2, 1, 16, [1, 6000], False),
+    (3, 2, 64, [0, 130, 4097], True),
+    (1, 1, 128, [20000], False),
+    (4, 1, 16, [63, 64, 65, 1], False),
+]
+
+
+@pytest.fixture
+def kernel_kind(request):
+    from decode_attention_paged_gb300 import api
+
+    default = api.get_decode_kernel()
+    api.set_decode_kernel(request.param)
+    yield request.param
+    api.set_decode_kernel(default)
+
+
+@pytest.mark.parametrize("kernel_kind", [0, 1, 2], indirect=True, ids=["pair", "single", "rail"])
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_kernel_parity(kernel_kind, case):
+    b, s_q, h_q, seqlens, causal = case
+    w = W.random_case(300 + CASES.index(case), b, s_q, h_q, seqlens, causal)
+    out, lse, _, _ = run_gpu(w)
+    ref_out, ref_lse = oracle.mla_decode(problem(w), nthreads=NTHREADS)
+    assert_close(out, lse, ref_out, ref_lse, f"kernel {kernel_kind} {case}")
+
+
+def test_kernels_agree_and_switch_needs_new_metadata():
+    from decode_attention_paged_gb300 import api
+
+    w = W.random_case(333, 3, 1, 16, [5000, 70, 900], False)
+    g = w.to("cuda")
+    default = api.get_decode_kernel()
+    try:
+        api.set_decode_kernel(api.KERNEL_PAIR)
+        meta_pair, ns_pair = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
+        o_pair, l_pair = api.mla_decode_fwd(g.q, g.k_cache, g.block_table, g.cache_seqlens,
+                                            w.softmax_scale, w.causal, meta_pair, ns_pair)
+        assert api.mla_last_device_error() == 0
+        api.set_decode_kernel(api.KERNEL_SINGLE)
+        meta_one, ns_one = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
+        o_one, l_one = api.mla_decode_fwd(g.q, g.k_cache, g.block_table, g.cache_seqlens,
+                                          w.softmax_scale, w.causal, meta_one, ns_one)
+        assert api.mla_last_device_error() == 0
+        # same function, different split plans and summation orders
+        d = (o_pair.float() - o_one.float()).abs().max().item()
+        assert d <= 2e-2, d
+        assert (l_pair - l_one).abs().max().item() <= 1e-3
+        if meta_pair.numel() != meta_one.numel():
+            # a plan for the pair kernel handed to the single-CTA kernel: its
+            # part count differs, which the kernel detects on the device
+            ws = torch.empty(api.workspace_size(w.b, w.h_q, w.s_q), dtype=torch.uint8,
+                             device="cuda")
+            out = torch.empty_like(o_one)
+            lse = torch.empty_like(l_one)
+            call = api.DecodeCall(g.q, g.k_cache, g.block_table, g.cache_seqlens, w.softmax_scale,
+                                  w.causal, meta_pair, ns_pair, ws, out, lse)
+            call.splitkv()
+            assert api.mla_last_device_error() == _lib.MLA_ERR_METADATA_MISMATCH
+        api.set_decode_kernel(api.KERNEL_RAIL)
+        meta_r, ns_r = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
+        o_r, l_r = api.mla_decode_fwd(g.q, g.k_cache, g.block_table, g.cache_seqlens,
+                                      w.softmax_scale, w.causal, meta_r, ns_r)
+        assert api.mla_last_device_error() == 0
+        assert (o_r.float() - o_one.float()).abs().max().item() <= 2e-2
+        assert (l_r - l_one).abs().max().item() <= 1e-3
+    finally:
+        api.set_decode_kernel(default)
+    assert api.get_decode_kernel() == default
