@@ -128,6 +128,18 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
+    // Same shared-memory carveout as the decode kernels (no SM reconfiguration
+    // between the kernels of one step).
+    static int carveout_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 31 || !(__atomic_load_n(&carveout_mask, __ATOMIC_RELAXED) & (1 << dev))) {
+        e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        if (dev < 31) __atomic_fetch_or(&carveout_mask, 1 << dev, __ATOMIC_RELAXED);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.R + kCombineWarps - 1) / kCombineWarps, p.batch, 1);
     cfg.blockDim = dim3(32 * kCombineWarps, 1, 1);

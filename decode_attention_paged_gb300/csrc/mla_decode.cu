@@ -26,9 +26,10 @@
 //   - S = Q K^T [64 x 64] goes to TMEM too (32 columns per buffer, two
 //     buffers): lanes 0..63 hold tokens 0..31 of each row, lanes 64..127
 //     tokens 32..63, so a row's max is combined from two threads.
-//   - Warp roles: warp 0 = TMA producer (one thread), warp 1 = TMEM owner and
-//     MMA issuer (one thread), warps 2..5 = softmax / correction / epilogue
-//     (one thread per TMEM lane).
+//   - Warp roles: warp 0 = TMA producer (lane 0 issues; the warp's lanes
+//     keep block-table entries loaded 32 pages ahead), warp 1 = TMEM owner
+//     and MMA issuer (converged warp, elect.sync), warps 2..5 = softmax /
+//     correction / epilogue (one thread per TMEM lane).
 //   - Q and each 64-token page are TMA-loaded as 9 chunks of [64 x 64] bf16
 //     with 128-byte swizzle; V is the first 8 chunks of the same page, read by
 //     the PV MMA as an MN-major operand, so the page is loaded once.
@@ -60,13 +61,6 @@ constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
 // own, so the drain has its own budget, independent of the (possibly tiny)
 // wait budget a caller set.
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
-#ifndef MLA_PREFETCH_PAGES
-#define MLA_PREFETCH_PAGES 0
-#endif
-// L2 prefetch distance in pages.  Off by default: measured on GB300, a 2-page
-// TMA ring already streams at the HBM limit and extra L2 prefetches only add
-// traffic; the read-ahead of block-table entries below is kept either way.
-constexpr uint32_t kPrefetchPages = MLA_PREFETCH_PAGES;
 #ifndef MLA_MMA_STRICT
 #define MLA_MMA_STRICT 0
 #endif
@@ -80,9 +74,6 @@ constexpr unsigned kIdleSleepNs = MLA_IDLE_SLEEP_NS;  // MMA issuer back-off whe
 #define MLA_XCH_SLEEP_NS 32
 #endif
 constexpr unsigned kXchSleepNs = MLA_XCH_SLEEP_NS;  // pair-exchange back-off
-constexpr uint32_t kReadAhead = 8;      // block-table entries read ahead of the loads
-constexpr int kPageRing = 16;           // ring of those entries (> kReadAhead)
-static_assert(kPrefetchPages <= kReadAhead && kReadAhead < kPageRing, "read-ahead ring");
 
 struct Barriers {
     uint64_t kv_full[kStages];
@@ -337,55 +328,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        // Loads run through a two-page ring; a second cursor kReadAhead pages
-        // ahead reads the block table early, so a load never waits for its
-        // page index (and, if kPrefetchPages > 0, asks L2 to fetch upcoming
-        // pages and the next request's Q tile).
+        // Loads run through a two-page ring.  The whole warp walks it (lane 0
+        // waits and issues the copies); block-table entries are loaded 32
+        // pages ahead, page g's by lane g % 32, and read with a shuffle when
+        // page g is issued, so a load never waits for its page index.
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
-        Cursor ld = cursor_begin(p, part), pf = ld;
-        int ring[kPageRing];
+        Cursor ld = cursor_begin(p, part), ahead = ld;
+        int bid = 0;
+        for (int i = 0; i < 32 && ahead.valid; ++i) {
+            if (lane == static_cast<int>(ahead.g & 31))
+                bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+            cursor_next(p, part, ahead);
+        }
         uint32_t n_kv = 0, n_q = 0;
         while (ld.valid) {
-            while (pf.valid && pf.g <= ld.g + kReadAhead) {
-                const int page = p.block_table[static_cast<int64_t>(pf.req) * p.bt_stride + pf.blk];
-                ring[pf.g % kPageRing] = page;
-                if (pf.g > ld.g && pf.g <= ld.g + kPrefetchPages)
-                    for (int c = 0; c < kChunks; ++c) tma_prefetch_l2_3d(&kv_map, 64 * c, 0, page);
-                if (kPrefetchPages > 0 && pf.blk == pf.b0 && pf.item > ld.item)
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_prefetch_l2_3d(&q_map, 64 * c, mtile * kTileM, pf.req);
-                cursor_next(p, part, pf);
-            }
+            const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
             const int st = ld.g & 1;
-            if (ld.g >= 2 &&
-                !mbar_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
-                break;
-            const int page = ring[ld.g % kPageRing];
-            mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-            uint8_t* dst = sKV + st * kStageBytes;
-            for (int c = 0; c < kChunks; ++c)
-                tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
-                            policy);
+            if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                uint8_t* dst = sKV + st * kStageBytes;
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
+                                policy);
+            }
+            __syncwarp();
             ++n_kv;
             if (ld.blk == ld.b0) {  // first block of a request: its Q tile
-                if (ld.item > 0 &&
-                    !mbar_wait(&bars->q_empty, (ld.item - 1) & 1, wc, MLA_ERR_DEVICE_TIMEOUT))
-                    break;
-                mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
-                                mtile * kTileM, ld.req, policy);
+                if (ld.item > 0 && !warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
+                                    mtile * kTileM, ld.req, policy);
+                }
+                __syncwarp();
                 ++n_q;
+            }
+            // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
+            if (ahead.valid) {
+                if (lane == static_cast<int>(ahead.g & 31))
+                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+                cursor_next(p, part, ahead);
             }
             cursor_next(p, part, ld);
         }
         // Drain: never leave the CTA with copies still landing in its smem.
-        for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)
-            mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
-        if (n_q > 0) mbar_drain(&bars->q_full, (n_q - 1) & 1, kDrainBudgetNs);
+        if (lane == 0) {
+            for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)
+                mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
+            if (n_q > 0) mbar_drain(&bars->q_full, (n_q - 1) & 1, kDrainBudgetNs);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         // Two cursors: QK^T of block g needs its page, its request's Q tile

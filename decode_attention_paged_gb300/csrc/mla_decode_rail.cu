@@ -74,6 +74,9 @@ namespace {
 #ifndef MLA_RAIL_PV_WARP
 #define MLA_RAIL_PV_WARP 7
 #endif
+#ifndef MLA_RAIL_LATE_SEMPTY  // release S only after the rail swap has been read
+#define MLA_RAIL_LATE_SEMPTY 1
+#endif
 constexpr int kProducerWarp = MLA_RAIL_PRODUCER_WARP;
 constexpr int kQkWarp = MLA_RAIL_QK_WARP;
 constexpr int kPvWarp = MLA_RAIL_PV_WARP;
@@ -96,15 +99,13 @@ constexpr uint32_t kColS = 416;  // 64 columns per lane group
 constexpr int kQkSteps = 20;
 constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
-constexpr uint32_t kReadAhead = 8;  // block-table entries read ahead
-constexpr int kPageRing = 16;
 
 struct Barriers {
     uint64_t kv_full[kMaxStages];
     uint64_t kv_empty[kMaxStages];
     uint64_t q_ready;  // this request's Q rails are in TMEM
     uint64_t s_full, s_empty;
-    uint64_t p_full, pv_done;
+    uint64_t p_full[2], pv_done[2];  // by page parity
     uint64_t o_free;
     uint64_t drain_qk, drain_pv;
 };
@@ -114,16 +115,18 @@ static_assert(sizeof(Barriers) <= 256, "barrier block");
 struct RailLayout {
     uint32_t n_stages;
     bool x_in_stage;  // rail swap through the page's RoPE chunk
+    bool p_in_stage;  // P (16 rows) and the swap share that chunk: P per stage
     uint32_t off_p, off_x, off_m, off_bar, off_misc, bytes;
 };
 __host__ __device__ constexpr RailLayout rail_layout(int q_box_rows) {
     RailLayout l{};
     l.x_in_stage = q_box_rows <= 32;
+    l.p_in_stage = q_box_rows <= 16;
     l.n_stages = l.x_in_stage ? 3u : 2u;
     l.off_p = l.n_stages * kStageBytes;
-    l.off_x = l.off_p + kPBytes;
+    l.off_x = l.off_p + (l.p_in_stage ? 0u : kPBytes);
     l.off_m = l.off_x + (l.x_in_stage ? 0u : 128u * 128u);  // 128 slots x 128 bytes
-    l.off_bar = l.off_m + 2560u;  // tagged swaps: uint2 v[2][128], then uint32 x tags[128]
+    l.off_bar = l.off_m + 512u;  // row max / row sum swap: float [128]
     l.off_misc = l.off_bar + 256u;                           // tmem base, abort flag
     l.bytes = l.off_misc + 64u;
     return l;
@@ -220,74 +223,6 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                  : "memory");
 }
 
-// Bounded spin until the partner's tag reaches `want`; warp-uniform verdict.
-__device__ __forceinline__ bool wait_tag(uint32_t tag_addr, uint32_t want, const WaitCtx& wc) {
-    bool ok = true;
-    uint32_t got;
-    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(got) : "r"(tag_addr) : "memory");
-    if (got != want) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t spin = 1;; ++spin) {
-            asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(got) : "r"(tag_addr) : "memory");
-            if (got == want) break;
-            if ((spin & 255) == 0) {
-                if (*wc.abort_flag) {
-                    ok = false;
-                    break;
-                }
-                if (globaltimer_ns() - t0 > wc.budget_ns) {
-                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-            }
-        }
-    }
-    __threadfence_block();
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Swap one float with the thread holding the other rail of the same row
-// (TMEM lane L <-> L ^ 64): value and tag go out in one 8-byte store, into
-// one of two slot sets chosen by the tag's parity, so that a slot is rewritten
-// only after the partner has answered the swap that read it.
-__device__ __forceinline__ bool swap_value(uint2* slot_sets, int lrow, uint32_t& seq, float v,
-                                           float& partner, const WaitCtx& wc) {
-    const uint32_t tag = ++seq;
-    uint2* slots = slot_sets + (tag & 1) * 128;
-    asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(slots + lrow)),
-                 "r"(__float_as_uint(v)), "r"(tag)
-                 : "memory");
-    const uint32_t src = smem_u32(slots + (lrow ^ 64));
-    bool ok = true;
-    uint2 got;
-    asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(got.x), "=r"(got.y) : "r"(src)
-                 : "memory");
-    if (got.y != tag) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t spin = 1;; ++spin) {
-            asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(got.x), "=r"(got.y)
-                         : "r"(src)
-                         : "memory");
-            if (got.y == tag) break;
-            if ((spin & 255) == 0) {
-                if (*wc.abort_flag) {
-                    ok = false;
-                    break;
-                }
-                if (globaltimer_ns() - t0 > wc.budget_ns) {
-                    raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-            }
-        }
-    }
-    partner = __uint_as_float(got.x);
-    return __all_sync(0xffffffffu, ok);
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -323,14 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->q_ready, n_active);
         mbar_init(&bars->s_full, 1);
         mbar_init(&bars->s_empty, n_active);
-        mbar_init(&bars->p_full, n_active);
-        mbar_init(&bars->pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->p_full[b], n_active);
+            mbar_init(&bars->pv_done[b], 1);
+        }
         mbar_init(&bars->o_free, n_active);
         mbar_init(&bars->drain_qk, 1);
         mbar_init(&bars->drain_pv, 1);
         fence_barrier_init();
-        uint32_t* tags = reinterpret_cast<uint32_t*>(smem + lay.off_m);
-        for (int i = 0; i < 2560 / 4; ++i) tags[i] = 0u;
         prefetch_tensormap(&q_map);
         prefetch_tensormap(&kv_map);
     }
@@ -376,50 +311,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
+        // The whole warp walks the ring; lane 0 waits and issues the copies.
+        // Block-table entries are loaded 32 pages ahead, page g's by lane
+        // g % 32, and read with a shuffle when page g is issued: the load has
+        // long landed by then, so the producer never stalls on it.
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
-        Cursor ld = cursor_begin(p, part), pf = ld;
-        int ring[kPageRing];
+        Cursor ld = cursor_begin(p, part), ahead = ld;
+        int bid = 0;
+        for (int i = 0; i < 32 && ahead.valid; ++i) {
+            if (lane == static_cast<int>(ahead.g & 31))
+                bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+            cursor_next(p, part, ahead);
+        }
         uint32_t n_issued = 0;  // ring entries issued
-        while (ld.valid) {
-            while (pf.valid && pf.g <= ld.g + kReadAhead) {
-                ring[pf.g % kPageRing] =
-                    p.block_table[static_cast<int64_t>(pf.req) * p.bt_stride + pf.blk];
-                cursor_next(p, part, pf);
-            }
-            bool stop = false;
+        bool stop = false;
+        while (ld.valid && !stop) {
+            const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
             // First block of a request: its Q tile goes into the ring first.
             for (int entry = (ld.blk == ld.b0) ? 0 : 1; entry < 2; ++entry) {
                 const uint32_t n = ld.ring() - 1 + entry;
                 const uint32_t st = n % n_stages;
-                if (n >= n_stages &&
-                    !mbar_wait(&bars->kv_empty[st], ((n / n_stages) + 1) & 1, wc,
-                               MLA_ERR_DEVICE_TIMEOUT)) {
+                if (n >= n_stages && !warp_wait(&bars->kv_empty[st], ((n / n_stages) + 1) & 1, wc)) {
                     stop = true;
                     break;
                 }
-                uint8_t* dst = sKV + st * kStageBytes;
-                if (entry == 0) {
-                    mbar_arrive_expect_tx(&bars->kv_full[st], q_bytes);
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(&q_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
-                                    mtile * kTileM, ld.req, policy);
-                } else {
-                    const int page = ring[ld.g % kPageRing];
-                    mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0,
-                                    page, policy);
+                if (lane == 0) {
+                    uint8_t* dst = sKV + st * kStageBytes;
+                    if (entry == 0) {
+                        mbar_arrive_expect_tx(&bars->kv_full[st], q_bytes);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(&q_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
+                                        mtile * kTileM, ld.req, policy);
+                    } else {
+                        mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
+                                        0, page, policy);
+                    }
                 }
+                __syncwarp();
                 n_issued = n + 1;
             }
             if (stop) break;
+            // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
+            if (ahead.valid) {
+                if (lane == static_cast<int>(ahead.g & 31))
+                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+                cursor_next(p, part, ahead);
+            }
             cursor_next(p, part, ld);
         }
-        for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k)
-            mbar_drain(&bars->kv_full[k % n_stages], (k / n_stages) & 1, kDrainBudgetNs);
+        if (lane == 0)
+            for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k)
+                mbar_drain(&bars->kv_full[k % n_stages], (k / n_stages) & 1, kDrainBudgetNs);
+        __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------ QK^T issuer
         // Page g needs its stage, its request's Q rails and a free S buffer.
@@ -464,16 +412,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous request's epilogue.
         constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
         const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
-        const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024);
+        // P: one buffer, or (16-row tiles) in each page's RoPE chunk
+        const uint64_t dP0 = lay.p_in_stage ? smem_desc(smem_u32(sKV + 8 * kChunkBytes), 16, 1024)
+                                            : smem_desc(smem_u32(sP), 16, 1024);
         constexpr uint64_t kStageUnits = kStageBytes >> 4;
         constexpr uint64_t kHalfUnits = (4 * kChunkBytes) >> 4;
         for (Cursor pv = cursor_begin(p, part); pv.valid; cursor_next(p, part, pv)) {
             const bool first = pv.blk == pv.b0;
             const uint32_t st = pv.ring() % n_stages;
-            if (!warp_wait(&bars->p_full, pv.g & 1, wc)) break;
+            if (!warp_wait(&bars->p_full[pv.g & 1], (pv.g >> 1) & 1, wc)) break;
             if (first && pv.item > 0 && !warp_wait(&bars->o_free, (pv.item - 1) & 1, wc)) break;
             tc_fence_after();
             const uint64_t bV = dV0 + st * kStageUnits;
+            const uint64_t dP = lay.p_in_stage ? dP0 + st * kStageUnits : dP0;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -483,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   bV + h * kHalfUnits + 128 * kk, idesc_pv,
                                   (first && kk == 0) ? 0u : 1u);
             if (elect_one()) {
-                mma_commit(&bars->pv_done);
+                mma_commit(&bars->pv_done[pv.g & 1]);
                 mma_commit(&bars->kv_empty[st]);
             }
             __syncwarp();
@@ -494,6 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (softmax_warp) {
         // -------------- rail swap / softmax / correction / epilogue / Q copy
+        // Warps q4 and q4 ^ 2 hold the two rails of the same rows and meet at
+        // a named barrier of their own for every swap.  Each leaves early
+        // only on a verdict both took from one barrier reduction
+        // (named_bar_and), so the two always pass the same barriers; every
+        // wait between barriers is bounded.
         const int q4 = warp;              // TMEM lane quadrant
         const int Lrow = 32 * q4 + lane;  // TMEM lane
         const int r = Lrow & 63, grp = Lrow >> 6;
@@ -501,14 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = r < rows_valid;
         const int s_idx = row / p.h_q, h_idx = row % p.h_q;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        const uint32_t pair_bar = 1 + (q4 & 1);  // warps q4 and q4 ^ 2
         const int me = n_active == 4 ? tid : (32 * (warp >> 1) + lane);  // among active threads
-        // Rail swap slots (128 bytes each, 16-byte units rotated by lane).
-        const int x_slot = lay.x_in_stage ? (lane + 32 * grp) : Lrow;
-        const int x_peer = lay.x_in_stage ? (lane + 32 * (grp ^ 1)) : (Lrow ^ 64);
-        uint2* v_swap = reinterpret_cast<uint2*>(smem + lay.off_m);  // [2][128] value + tag
-        const uint32_t x_tag_own = smem_u32(smem + lay.off_m + 2048 + Lrow * 4);
-        const uint32_t x_tag_peer = smem_u32(smem + lay.off_m + 2048 + (Lrow ^ 64) * 4);
-        uint32_t vseq = 0, xseq = 0;
+        // Rail swap slots (128 bytes each, 16-byte units rotated by lane):
+        // 16-row tiles use 32 slots after P's 16 rows in the page's RoPE
+        // chunk, 32-row tiles 64 slots there, larger tiles a buffer of 128.
+        const int x_slot = lay.p_in_stage   ? ((lane & 15) + 16 * grp)
+                           : lay.x_in_stage ? (lane + 32 * grp)
+                                            : Lrow;
+        const int x_peer = lay.p_in_stage   ? ((lane & 15) + 16 * (grp ^ 1))
+                           : lay.x_in_stage ? (lane + 32 * (grp ^ 1))
+                                            : (Lrow ^ 64);
+        const uint32_t x_off = 8 * kChunkBytes + (lay.p_in_stage ? 16 * 128 : 0);
+        float* v_slot = reinterpret_cast<float*>(smem + lay.off_m);  // [128] row max / row sum
         uint32_t gblk = 0, item = 0;
         bool alive = true;
         for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
@@ -527,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Q tile of this request: from its ring stage into the rails.
                 const uint32_t nq = gblk + item;
                 const uint32_t stq = nq % n_stages;
-                if (!warp_wait(&bars->kv_full[stq], (nq / n_stages) & 1, wc)) {
+                if (!named_bar_and(pair_bar, 64,
+                                   warp_wait(&bars->kv_full[stq], (nq / n_stages) & 1, wc))) {
                     alive = false;
                     break;
                 }
@@ -557,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t n = gblk + item + 1;
                 const uint32_t st = n % n_stages;
                 uint8_t* stage = sKV + st * kStageBytes;
-                if (!warp_wait(&bars->s_full, gblk & 1, wc)) {
+                if (!named_bar_and(pair_bar, 64, warp_wait(&bars->s_full, gblk & 1, wc))) {
                     alive = false;
                     break;
                 }
@@ -567,37 +529,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tl + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
                 tmem_ld_wait();
                 tc_fence_before();
-                warp_arrive(&bars->s_empty);
+                if (!MLA_RAIL_LATE_SEMPTY) warp_arrive(&bars->s_empty);
 
                 // Swap rail partials with the thread holding the other rail of
                 // this row: rail 0 keeps tokens 0..31, rail 1 tokens 32..63.
+                // (Padding rows skip it; their partner is padding too.)
                 const uint32_t x_base =
-                    lay.x_in_stage ? smem_u32(stage + 8 * kChunkBytes) : smem_u32(smem + lay.off_x);
+                    lay.x_in_stage ? smem_u32(stage + x_off) : smem_u32(smem + lay.off_x);
                 const uint32_t send = x_base + x_slot * 128, recv = x_base + x_peer * 128;
                 // the tokens the partner keeps: rail 0 gives 32..63, rail 1 gives 0..31
                 const bool g0 = grp == 0;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < 8 && row_valid; ++k) {
                     const uint32_t u = (k ^ (lane & 7)) * 16;
                     st_shared_v4(send + u, g0 ? own[32 + 4 * k] : own[4 * k],
                                  g0 ? own[33 + 4 * k] : own[4 * k + 1],
                                  g0 ? own[34 + 4 * k] : own[4 * k + 2],
                                  g0 ? own[35 + 4 * k] : own[4 * k + 3]);
                 }
-                __threadfence_block();
-                asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(x_tag_own), "r"(++xseq)
-                             : "memory");
-                if (!wait_tag(x_tag_peer, xseq, wc)) {
-                    alive = false;
-                    break;
-                }
+                named_bar_sync(pair_bar, 64);
                 uint32_t other[32];
+                if (row_valid) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t u = (k ^ (lane & 7)) * 16;
-                    ld_shared_v4(recv + u, other[4 * k], other[4 * k + 1], other[4 * k + 2],
-                                 other[4 * k + 3]);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t u = (k ^ (lane & 7)) * 16;
+                        ld_shared_v4(recv + u, other[4 * k], other[4 * k + 1], other[4 * k + 2],
+                                     other[4 * k + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) other[k] = 0u;
                 }
+                if (MLA_RAIL_LATE_SEMPTY) warp_arrive(&bars->s_empty);
                 const int keep = grp == 0 ? 0 : 32;
                 const int t0 = blk * kPage + keep;
                 float x[32];
@@ -609,12 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     x[c] = (row_valid && t0 + c < lim) ? (r0 + r1) * p.scale_log2 : -INFINITY;
                     hmax = fmaxf(hmax, x[c]);
                 }
-                float pmax;
-                if (!swap_value(v_swap, Lrow, vseq, hmax, pmax, wc)) {
-                    alive = false;
-                    break;
-                }
-                const float tmax = fmaxf(hmax, pmax);
+                // Row max over both halves (the slot is rewritten only after
+                // the next barrier, which the partner passes after reading it).
+                v_slot[Lrow] = hmax;
+                named_bar_sync(pair_bar, 64);
+                const float tmax = fmaxf(hmax, v_slot[Lrow ^ 64]);
                 float alpha = 1.f;
                 bool need = false;
                 if (tmax > m_used + kLazyThreshold) {
@@ -635,13 +597,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_part += psum;
 
-                // P and O are single buffers: PV(g - 1) must be done.
-                if (gblk > 0 && !warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                // O is rescaled after PV(g - 1), and a single P buffer is
+                // rewritten after PV(g - 1) too.  Per-stage P needs neither,
+                // but PV may trail by at most two pages: the parity waits on
+                // the two p_full / pv_done barriers stay unambiguous.  (The
+                // two warps of a pair see the same rows, hence the same
+                // rescale decision.)
+                const bool rescale = __any_sync(0xffffffffu, need && blk > b0);
+                const uint32_t lag = (rescale || !lay.p_in_stage) ? 1u : 2u;
+                bool ok = true;
+                if (gblk >= lag) {
+                    const uint32_t w = gblk - lag;
+                    ok = warp_wait(&bars->pv_done[w & 1], (w >> 1) & 1, wc);
+                }
+                if (!named_bar_and(pair_bar, 64, ok)) {
                     alive = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need && blk > b0)) {
+                if (rescale) {
                     const float a = (need && blk > b0) ? alpha : 1.f;
 #pragma unroll 1
                     for (int cg = 0; cg < 8; ++cg) {
@@ -665,32 +639,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(0, 0, 0, 0);
                     }
                 }
+                // (per-stage P holds rows 0..15 only; the swap slots follow)
+                uint8_t* pbuf = lay.p_in_stage ? stage + 8 * kChunkBytes : sP;
+                if (!lay.p_in_stage || r < 16) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t off = sw128_offset(r, 4 * grp + k);
-                    *reinterpret_cast<uint4*>(sP + off) =
-                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t off = sw128_offset(r, 4 * grp + k);
+                        *reinterpret_cast<uint4*>(pbuf + off) =
+                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                warp_arrive(&bars->p_full);
+                warp_arrive(&bars->p_full[gblk & 1]);
             }
             if (!alive) break;
 
             // ---------------------------------------------------- epilogue
             float l_tot = 0.f;
             if (has_blocks) {
-                if (!warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                if (!named_bar_and(pair_bar, 64,
+                                   warp_wait(&bars->pv_done[(gblk - 1) & 1],
+                                             ((gblk - 1) >> 1) & 1, wc))) {
                     alive = false;
                     break;
                 }
                 tc_fence_after();
-                float l_other;
-                if (!swap_value(v_swap, Lrow, vseq, l_part, l_other, wc)) {
-                    alive = false;
-                    break;
-                }
-                l_tot = l_part + l_other;
+                v_slot[Lrow] = l_part;
+                named_bar_sync(pair_bar, 64);
+                l_tot = l_part + v_slot[Lrow ^ 64];
             }
             const bool empty = !(l_tot > 0.f);
             const float inv = empty ? 0.f : 1.f / l_tot;

@@ -153,6 +153,18 @@ cudaError_t launch_sched(const int32_t* seqlens, int batch, int R, int num_parts
                          int fixed_overhead, int32_t* meta, int32_t* num_splits,
                          cudaStream_t stream) {
     const size_t smem = 2 * sizeof(int32_t) * (static_cast<size_t>(batch) + 1);
+    // Same shared-memory carveout as the decode kernels, so that a step's
+    // kernels follow one another without reconfiguring the SMs.
+    static int carveout_mask = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    if (dev >= 31 || !(__atomic_load_n(&carveout_mask, __ATOMIC_RELAXED) & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(sched_kernel,
+                                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        if (dev < 31) __atomic_fetch_or(&carveout_mask, 1 << dev, __ATOMIC_RELAXED);
+    }
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(sched_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,

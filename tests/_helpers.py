@@ -64,6 +64,7 @@ def sample_units(w: W.Workload, n: int, seed: int):
     for i in {0, w.b - 1, int(np.argmax(L)), int(np.argmin(L))}:
         for rho in {0, R - 1, R // 2, min(R - 1, 63), min(R - 1, 64)}:
             units.add((i, rho))
+    n = min(n, w.b * R)  # there are only b * R distinct units
     while len(units) < n:
         units.add((int(rng.integers(0, w.b)), int(rng.integers(0, R))))
     return np.array(sorted(units), dtype=np.int32)

@@ -20,6 +20,11 @@ CASES = [
     (3, 2, 64, [0, 130, 4097], True),
     (1, 1, 128, [20000], False),
     (4, 1, 16, [63, 64, 65, 1], False),
+    # many short pieces per SM part (several requests in one part): the
+    # softmax may run ahead of PV by two pages on the per-stage-P path
+    (8, 1, 16, [4096] * 8, False),
+    (128, 1, 16, [512] * 128, False),
+    (24, 2, 16, [700] * 24, True),
 ]
 
 
