@@ -58,8 +58,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel", choices=["single", "pair", "rail"], default="single",
-                    help="decode kernel: single CTA (default), 2-CTA cluster pair, or two-rail")
+    ap.add_argument("--kernel", choices=["auto", "single", "pair", "tq"], default="auto",
+                    help="decode kernel: auto (default: tq for s_q*h_q <= 32, else single), "
+                         "single CTA, 2-CTA cluster pair, or Q in TMEM")
     return ap.parse_args()
 
 
@@ -82,7 +83,7 @@ def load_peaks():
 
 KERNEL_SOURCES = {"pair": ("decode_pair_kernel", "decode_attention_paged_gb300/csrc/mla_decode_pair.cu"),
                   "single": ("decode_kernel", "decode_attention_paged_gb300/csrc/mla_decode.cu"),
-                  "rail": ("decode_rail_kernel", "decode_attention_paged_gb300/csrc/mla_decode_rail.cu")}
+                  "tq": ("decode_tq_kernel", "decode_attention_paged_gb300/csrc/mla_decode_tq.cu")}
 
 
 def kernel_source_hash(kernel="single"):
@@ -430,8 +431,9 @@ def main():
     from decode_attention_paged_gb300 import api
     from decode_attention_paged_gb300 import workloads as W_mod
 
-    api.set_decode_kernel({"single": api.KERNEL_SINGLE, "pair": api.KERNEL_PAIR,
-                           "rail": api.KERNEL_RAIL}[args.kernel])
+    api.set_decode_kernel({"auto": api.KERNEL_AUTO, "single": api.KERNEL_SINGLE,
+                           "pair": api.KERNEL_PAIR,
+                           "tq": api.KERNEL_TQ}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     # weak scaling: every rank decodes its own batch of requests (replicas).
     w = W_mod.CONFIGS[args.workload](seed_offset=1000 * rank)
@@ -466,10 +468,11 @@ def main():
     clocks = sampler.summary() if sampler else None
     dec_ms = res["ms_decode"]
     achieved = res["bytes"] / (dec_ms * 1e-3) / 1e9
-    traffic = profile_traffic(args.workload, args.kernel)
+    kname = args.kernel if args.kernel != "auto" else ("tq" if w.s_q * w.h_q <= 32 else "single")
+    traffic = profile_traffic(args.workload, kname)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": KERNEL_SOURCES[args.kernel][0] + " (split-KV)", "peak_source": peak_src,
+                "kernel": KERNEL_SOURCES[kname][0] + " (split-KV)", "peak_source": peak_src,
                 "tensor_frac_of_bf16_peak": res["flops"] / (dec_ms * 1e-3) / 1e12 / bf16_peak,
                 "ms_per_launch": dec_ms, "launches_timed": res["kernel_steps"]}
 

@@ -180,8 +180,9 @@ def set_fixed_overhead(blocks: int) -> None:
 
 
 KERNEL_PAIR = 0    # one 2-CTA cluster per SM pair, head dims split across the pair
-KERNEL_SINGLE = 1  # one CTA per SM holding all 576 dims (default)
-KERNEL_RAIL = 2    # one CTA per SM, Q in tensor memory, two-rail QK^T
+KERNEL_SINGLE = 1  # one CTA per SM holding all 576 dims
+KERNEL_TQ = 2      # one CTA per SM, most of Q in tensor memory, three KV stages
+KERNEL_AUTO = 3    # default: KERNEL_TQ for s_q * h_q <= 32, else KERNEL_SINGLE
 
 
 def set_decode_kernel(kind: int) -> None:

@@ -25,7 +25,7 @@ constexpr int kDefaultFixedOverhead = 2;
 
 std::atomic<uint64_t> g_budget_ns{kDefaultBudgetNs};
 std::atomic<int> g_fixed_overhead{kDefaultFixedOverhead};
-std::atomic<int> g_kernel{MLA_KERNEL_SINGLE};
+std::atomic<int> g_kernel{MLA_KERNEL_AUTO};
 
 struct DeviceInfo {
     std::once_flag once;
@@ -155,7 +155,8 @@ int mla_set_wait_budget_ns(uint64_t budget_ns) {
 }
 
 int mla_set_decode_kernel(int kind) {
-    if (kind != MLA_KERNEL_PAIR && kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_RAIL)
+    if (kind != MLA_KERNEL_PAIR && kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_TQ &&
+        kind != MLA_KERNEL_AUTO)
         return MLA_ERR_INVALID_ARGUMENT;
     g_kernel.store(kind);
     return MLA_OK;
@@ -324,9 +325,11 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.budget_ns = g_budget_ns.load();
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int kind = g_kernel.load();
+    int kind = g_kernel.load();
+    if (kind == MLA_KERNEL_AUTO)  // Q mostly in TMEM wins for tiles of at most 32 rows
+        kind = R <= 32 ? MLA_KERNEL_TQ : MLA_KERNEL_SINGLE;
     cudaError_t e = kind == MLA_KERNEL_PAIR   ? launch_decode_pair(p, q_map, kv_map, s)
-                    : kind == MLA_KERNEL_RAIL ? launch_decode_rail(p, q_map, kv_map, s)
+                    : kind == MLA_KERNEL_TQ   ? launch_decode_tq(p, q_map, kv_map, s)
                                               : launch_decode(p, q_map, kv_map, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

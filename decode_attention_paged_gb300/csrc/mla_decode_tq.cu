@@ -1,5 +1,5 @@
-// mla_decode_rail.cu -- split-KV paged MLA decode for sm_103a with the query
-// tile in tensor memory and QK^T as a two-rail weight-stationary GEMM.
+// mla_decode_tq.cu -- split-KV paged MLA decode for sm_103a with most of the
+// query tile in tensor memory, so that three KV pages fit in shared memory.
 //
 // Sources (web pages, cited by title and section):
 //   [Overview] "[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐":
@@ -7,11 +7,9 @@
 //       sec. 4 (paged KV through block_table), sec. 6 (split-KV partials),
 //       sec. 7 (online softmax makes the partials mergeable).
 //   [Rails] "Blackwell 多轨矩乘(multi-rail GEMM):FlashMLA 如何用一条 MMA 算完两路
-//       QK", sec. 1.2 (M=64 .ws: lane group g multiplies its own A rows by
-//       the g-th half of B's N), sec. 2.1-2.3 (store different feature dims
-//       of Q in the two lane groups, reinterpret one KV tile as 2T rows of
-//       half the dims, add the two partial score tiles after masking),
-//       sec. 3.2 (the saving is tensor memory, not multiplications).
+//       QK", sec. 1.2-1.5 (M=64 .ws: each lane group reads its own copy of an
+//       A operand held in tensor memory), sec. 1.5 (that copy's cost in TMEM
+//       columns is what limits how much of Q fits).
 //   [DeepDive] "FlashMLA 新内核深度解析：Seesaw 调度、细粒度 TMA 流水线与 H800
 //       上的 660 TFlops MLA 解码": "细粒度 TMA copy-GEMM 流水线" (a 64x576 K
 //       tile moves as 64x64 TMA copies), "缓存提示" (EVICT_FIRST), the exp ->
@@ -19,45 +17,38 @@
 //       Launch", "Tile Scheduler" (each SM part walks its DecodingSchedMeta).
 //   [AttnBook] "3.4 Attention kernel": "在线 softmax", 代码 (causal mask).
 //
-// Why this shape.  A 64 x 576 bf16 Q tile held in shared memory (72 KB) next
-// to 72 KB KV pages leaves room for two pages in flight, and on sm_103a the
-// per-SM bandwidth share needs more: every page waits out an HBM round trip
-// plus QK^T -> softmax -> PV before its buffer is refilled.  Here Q lives in
-// tensor memory as the A operand of QK^T, so shared memory holds three pages
-// (two when the query tile has more than 32 rows and the rail exchange needs a
-// buffer of its own).  Q in tensor memory would need 288 columns per lane
-// group as the replicated operand of a plain weight-stationary MMA -- with the
-// 256 columns of O that is more than the 512 there are -- so the two lane
-// groups hold different dims of Q (two rails):
-//   k-step j = 4 p + kk (p < 4): rail 0 = dims of chunk 2p, rail 1 = chunk 2p+1
-//   k-step 16 + kk:              rail 0 = zero, rail 1 = the RoPE chunk 8
-// with the 16 dims [16 kk, 16 kk + 16) of the chunk each.  One MMA with N =
-// 128 reads B rows 0..63 from chunk c and rows 64..127 from chunk c + 1 of
-// the same page (chunks are 8 KB apart), so every KV page is read once, as
-// stored; the RoPE steps use chunk 7 as rail 0's partner, multiplied by the
-// zero rail-0 Q.  Lane group g ends with the partial scores of rail g for
-// all 64 tokens; the two partials of a row are added by the softmax threads
-// after a swap through shared memory (for tiles of at most 32 rows the swap
-// uses the page's RoPE chunk, dead once QK^T is done), rail 0 first, and a
-// masked token takes -inf before any addition.
+// Why this shape.  On GB300 one SM must take in a 72 KB page about every
+// 1.6 us to keep HBM busy, and a page stays in shared memory from its TMA
+// landing until PV has read it: QK^T, softmax and PV in a row, about 2 us.
+// With the 72 KB Q tile in shared memory only two pages fit, so loads stall.
+// Here Q's dims 0..447 live in tensor memory as the A operand of QK^T (the
+// weight-stationary TS form reads a copy per lane group, so the copy takes
+// 224 columns next to O's 256 and S's 32), and only dims 448..575 (two 64-dim
+// chunks) stay in shared memory, packed to the rows the tile has.  For tiles
+// of at most 32 rows that leaves room for three pages; larger tiles keep two.
+// P goes into each page's RoPE chunk, which QK^T is done with, so P has one
+// buffer per stage.
 //
 // Tensor memory (512 columns): O [64 x 512] fp32 as two weight-stationary
 // N=256 halves at columns 0 and 128 (lanes 0..63 dims 256h + [0,128), lanes
-// 64..127 dims 256h + [128,256)); Q rails at 256..415 (20 k-steps x 8
-// columns, bf16 pairs); S partials at 416..479 (64 columns per lane group).
+// 64..127 dims 256h + [128,256)); Q dims 0..447 at 256..479 (28 k-steps x 8
+// columns of bf16 pairs, the same rows in both lane groups); S [64 x 64] at
+// 480..511 (lanes 0..63 tokens 0..31 of their row, lanes 64..127 tokens
+// 32..63).
 //
-// The query tile arrives through the KV ring as a pseudo page (the producer
-// puts each request's Q tile in the ring ahead of its pages); the softmax
-// threads move their rows from the swizzled stage into their TMEM lanes.
+// The query tile arrives through the KV ring as a pseudo page ahead of its
+// request's pages; the softmax threads move it into tensor memory (dims
+// 0..447) and into the packed shared-memory chunks (dims 448..575).
 //
 // Warp roles (warp w runs on SM sub-partition w % 4 and reaches TMEM lanes
-// 32 (w % 4) .. + 31): warps 0..3 softmax / rail swap / correction / epilogue
+// 32 (w % 4) .. + 31): warps 0..3 softmax / correction / epilogue / Q copy
 // (one thread per TMEM lane; for tiles of at most 32 valid rows only warps 0
-// and 2 take part), warp 4 TMA producer (one thread), warp 5 TMEM owner and
-// QK^T issuer, warp 7 PV issuer (elect.sync issue from converged warps).
-//
-// Every wait is bounded; a timeout records MLA_ERR_DEVICE_TIMEOUT, drains the
-// CTA's own copies and MMAs, frees TMEM and returns.
+// and 2 take part), warp 4 TMA producer, warp 5 TMEM owner and QK^T issuer,
+// warp 7 PV issuer.  The two warps that hold the halves of the same rows
+// exchange row maxima at a named barrier of their own and agree on every
+// early exit through a barrier reduction, so they always pass the same
+// barriers.  Every wait is bounded; a timeout records MLA_ERR_DEVICE_TIMEOUT,
+// drains the CTA's own copies and MMAs, frees TMEM and returns.
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -65,45 +56,26 @@ namespace mla {
 
 namespace {
 
-#ifndef MLA_RAIL_PRODUCER_WARP
-#define MLA_RAIL_PRODUCER_WARP 4
-#endif
-#ifndef MLA_RAIL_QK_WARP
-#define MLA_RAIL_QK_WARP 5
-#endif
-#ifndef MLA_RAIL_PV_WARP
-#define MLA_RAIL_PV_WARP 7
-#endif
-#ifndef MLA_RAIL_LATE_SEMPTY  // release S only after the rail swap has been read
-#define MLA_RAIL_LATE_SEMPTY 1
-#endif
-constexpr int kProducerWarp = MLA_RAIL_PRODUCER_WARP;
-constexpr int kQkWarp = MLA_RAIL_QK_WARP;
-constexpr int kPvWarp = MLA_RAIL_PV_WARP;
-constexpr int kMaxRoleWarp =
-    kProducerWarp > kQkWarp ? (kProducerWarp > kPvWarp ? kProducerWarp : kPvWarp)
-                            : (kQkWarp > kPvWarp ? kQkWarp : kPvWarp);
-constexpr int kThreads = 32 * (kMaxRoleWarp + 1);
-static_assert(kProducerWarp >= 4 && kQkWarp >= 4 && kPvWarp >= 4 && kProducerWarp != kQkWarp &&
-                  kProducerWarp != kPvWarp && kQkWarp != kPvWarp,
-              "warp roles overlap the softmax warps or each other");
+constexpr int kProducerWarp = 4;
+constexpr int kQkWarp = 5;
+constexpr int kPvWarp = 7;
+constexpr int kThreads = 256;
 
 constexpr int kMaxStages = 3;
 constexpr uint32_t kStageBytes = kChunks * kChunkBytes;  // 73728
-constexpr uint32_t kPBytes = 64 * 128;                   // P [64 rows x 64 tokens] bf16
 constexpr uint32_t kSmemMax = 232448;                    // 227 KB per CTA
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // two PV halves of 128 columns
-constexpr uint32_t kColQ = 256;  // 20 k-steps x 8 columns
-constexpr uint32_t kColS = 416;  // 64 columns per lane group
-constexpr int kQkSteps = 20;
+constexpr uint32_t kColQ = 256;  // Q dims 0..447: 28 k-steps x 8 columns
+constexpr uint32_t kColS = 480;  // S: 32 columns
+constexpr int kTmemChunks = 7;   // 64-dim chunks of Q held in tensor memory
 constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
 
 struct Barriers {
     uint64_t kv_full[kMaxStages];
     uint64_t kv_empty[kMaxStages];
-    uint64_t q_ready;  // this request's Q rails are in TMEM
+    uint64_t q_ready;  // this request's Q tile is in TMEM and in the packed chunks
     uint64_t s_full, s_empty;
     uint64_t p_full[2], pv_done[2];  // by page parity
     uint64_t o_free;
@@ -111,29 +83,29 @@ struct Barriers {
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 
-// Shared-memory layout as a function of the rows one Q tile load brings.
-struct RailLayout {
-    uint32_t n_stages;
-    bool x_in_stage;  // rail swap through the page's RoPE chunk
-    bool p_in_stage;  // P (16 rows) and the swap share that chunk: P per stage
-    uint32_t off_p, off_x, off_m, off_bar, off_misc, bytes;
+// Shared-memory layout as a function of the rows one Q tile load brings: the
+// two packed Q chunks (q_rows rows each; the M=64 MMA still reads 64 rows per
+// chunk, and the rows past q_rows -- the next chunk's, or the first stage's --
+// are padding rows whose scores the softmax masks), then the KV stages.
+struct TqLayout {
+    uint32_t q_rows, n_stages;
+    uint32_t off_kv, off_v, off_bar, off_misc, bytes;
 };
-__host__ __device__ constexpr RailLayout rail_layout(int q_box_rows) {
-    RailLayout l{};
-    l.x_in_stage = q_box_rows <= 32;
-    l.p_in_stage = q_box_rows <= 16;
-    l.n_stages = l.x_in_stage ? 3u : 2u;
-    l.off_p = l.n_stages * kStageBytes;
-    l.off_x = l.off_p + (l.p_in_stage ? 0u : kPBytes);
-    l.off_m = l.off_x + (l.x_in_stage ? 0u : 128u * 128u);  // 128 slots x 128 bytes
-    l.off_bar = l.off_m + 512u;  // row max / row sum swap: float [128]
-    l.off_misc = l.off_bar + 256u;                           // tmem base, abort flag
+__host__ __device__ constexpr TqLayout tq_layout(int q_box_rows) {
+    TqLayout l{};
+    l.q_rows = q_box_rows <= 16 ? 16u : (q_box_rows <= 32 ? 32u : 64u);
+    l.n_stages = l.q_rows <= 32 ? 3u : 2u;
+    l.off_kv = 2u * l.q_rows * 128u;  // a multiple of 1024
+    l.off_v = l.off_kv + l.n_stages * kStageBytes;  // row max / row sum swap: float[128]
+    l.off_bar = l.off_v + 512u;
+    l.off_misc = l.off_bar + 256u;  // tmem base, abort flag
     l.bytes = l.off_misc + 64u;
     return l;
 }
-static_assert(rail_layout(16).bytes <= kSmemMax && rail_layout(32).bytes <= kSmemMax &&
-                  rail_layout(64).bytes <= kSmemMax,
+static_assert(tq_layout(16).bytes <= kSmemMax && tq_layout(32).bytes <= kSmemMax &&
+                  tq_layout(64).bytes <= kSmemMax,
               "exceeds the 227 KB per-CTA shared memory limit");
+static_assert(tq_layout(32).n_stages == 3 && tq_layout(64).n_stages == 2, "stage counts");
 static_assert(kSmemMax < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
 
 struct Part {
@@ -226,13 +198,13 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_rail_kernel(const __grid_constant__ DecodeParams p,
-                       const __grid_constant__ CUtensorMap q_map,
-                       const __grid_constant__ CUtensorMap kv_map) {
+    decode_tq_kernel(const __grid_constant__ DecodeParams p,
+                     const __grid_constant__ CUtensorMap q_map,
+                     const __grid_constant__ CUtensorMap kv_map) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int mtile = blockIdx.x, part_idx = blockIdx.y;
-    const RailLayout lay = rail_layout(p.q_box_rows);
+    const TqLayout lay = tq_layout(p.q_box_rows);
     const uint32_t n_stages = lay.n_stages;
     int rows_valid = p.R - mtile * kTileM;
     rows_valid = rows_valid > kTileM ? kTileM : rows_valid;
@@ -241,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t n_active = rows_valid > 32 ? 4u : 2u;
     const bool softmax_warp = warp < 4 && (n_active == 4 || (warp & 1) == 0);
 
-    uint8_t* sKV = smem;
-    uint8_t* sP = smem + lay.off_p;
+    uint8_t* sQr = smem;  // packed Q chunks 7 and 8
+    uint8_t* sKV = smem + lay.off_kv;
     Barriers* bars = reinterpret_cast<Barriers*>(smem + lay.off_bar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.off_misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.off_misc + 4);
@@ -370,18 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------ QK^T issuer
-        // Page g needs its stage, its request's Q rails and a free S buffer.
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 128, false, false);
+        // Page g needs its stage, its request's Q tile and a free S buffer.
+        // 28 TS MMAs over dims 0..447 (A from TMEM), 8 SS MMAs over 448..575
+        // (A from the packed chunks), all N = 64 into S.
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
         const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024);
+        const uint64_t dQr = smem_desc(smem_u32(sQr), 16, 1024);
         constexpr uint64_t kStageUnits = kStageBytes >> 4;
         constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
+        const uint64_t q_chunk_units = (lay.q_rows * 128u) >> 4;
         const uint32_t tS = tmem + kColS, tQ = tmem + kColQ;
         for (Cursor qk = cursor_begin(p, part); qk.valid; cursor_next(p, part, qk)) {
             const uint32_t n = qk.ring();
             const uint32_t st = n % n_stages;
             if (qk.blk == qk.b0) {
-                // The softmax warps copied this request's Q tile into the
-                // rails; its ring stage (the entry before this page) is free.
+                // The softmax warps copied this request's Q tile; its ring
+                // stage (the entry before this page) is free.
                 if (!warp_wait(&bars->q_ready, qk.item & 1, wc)) break;
                 if (lane == 0) mbar_arrive(&bars->kv_empty[(n - 1) % n_stages]);
             }
@@ -390,14 +366,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t bK = dK0 + st * kStageUnits;
 #pragma unroll
-            for (int j = 0; j < kQkSteps; ++j) {
-                const int pair = j < 16 ? j / 4 : 0;
-                const int kk = j & 3;
-                // rail 0 chunk (rail 1 reads the chunk 8 KB after it)
-                const uint64_t chunk = j < 16 ? 2 * pair : 7;
+            for (int j = 0; j < 4 * kTmemChunks; ++j)
                 if (elect_one())
-                    mma_ws_ts(tS, tQ + 8 * j, bK + chunk * kChunkUnits + 2 * kk, idesc_qk,
+                    mma_ws_ts(tS, tQ + 8 * j, bK + (j / 4) * kChunkUnits + 2 * (j & 3), idesc_qk,
                               j ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = kTmemChunks + j / 4;  // 7, 8
+                if (elect_one())
+                    mma_ws_ss(tS, dQr + (j / 4) * q_chunk_units + 2 * (j & 3),
+                              bK + c * kChunkUnits + 2 * (j & 3), idesc_qk, 1u);
             }
             if (elect_one()) mma_commit(&bars->s_full);
             __syncwarp();
@@ -408,13 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------ PV issuer
-        // Page g needs P(g) and, on a request's first block, O released by
-        // the previous request's epilogue.
+        // Page g needs P(g) (in its stage's RoPE chunk) and, on a request's
+        // first block, O released by the previous request's epilogue.
         constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
         const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
-        // P: one buffer, or (16-row tiles) in each page's RoPE chunk
-        const uint64_t dP0 = lay.p_in_stage ? smem_desc(smem_u32(sKV + 8 * kChunkBytes), 16, 1024)
-                                            : smem_desc(smem_u32(sP), 16, 1024);
+        const uint64_t dP0 = smem_desc(smem_u32(sKV + 8 * kChunkBytes), 16, 1024);
         constexpr uint64_t kStageUnits = kStageBytes >> 4;
         constexpr uint64_t kHalfUnits = (4 * kChunkBytes) >> 4;
         for (Cursor pv = cursor_begin(p, part); pv.valid; cursor_next(p, part, pv)) {
@@ -424,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (first && pv.item > 0 && !warp_wait(&bars->o_free, (pv.item - 1) & 1, wc)) break;
             tc_fence_after();
             const uint64_t bV = dV0 + st * kStageUnits;
-            const uint64_t dP = lay.p_in_stage ? dP0 + st * kStageUnits : dP0;
+            const uint64_t dP = dP0 + st * kStageUnits;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -444,32 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_drain(&bars->drain_pv, 0, kDrainBudgetNs);
         __syncwarp();
     } else if (softmax_warp) {
-        // -------------- rail swap / softmax / correction / epilogue / Q copy
-        // Warps q4 and q4 ^ 2 hold the two rails of the same rows and meet at
-        // a named barrier of their own for every swap.  Each leaves early
-        // only on a verdict both took from one barrier reduction
-        // (named_bar_and), so the two always pass the same barriers; every
-        // wait between barriers is bounded.
+        // ---------------- softmax / correction / epilogue / Q copy
         const int q4 = warp;              // TMEM lane quadrant
         const int Lrow = 32 * q4 + lane;  // TMEM lane
-        const int r = Lrow & 63, grp = Lrow >> 6;
+        const int r = Lrow & 63, half = Lrow >> 6;
         const int row = mtile * kTileM + r;
         const bool row_valid = r < rows_valid;
         const int s_idx = row / p.h_q, h_idx = row % p.h_q;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-        const uint32_t pair_bar = 1 + (q4 & 1);  // warps q4 and q4 ^ 2
+        const uint32_t pair_bar = 1 + (q4 & 1);  // warps q4 and q4 ^ 2: the two halves of a row
         const int me = n_active == 4 ? tid : (32 * (warp >> 1) + lane);  // among active threads
-        // Rail swap slots (128 bytes each, 16-byte units rotated by lane):
-        // 16-row tiles use 32 slots after P's 16 rows in the page's RoPE
-        // chunk, 32-row tiles 64 slots there, larger tiles a buffer of 128.
-        const int x_slot = lay.p_in_stage   ? ((lane & 15) + 16 * grp)
-                           : lay.x_in_stage ? (lane + 32 * grp)
-                                            : Lrow;
-        const int x_peer = lay.p_in_stage   ? ((lane & 15) + 16 * (grp ^ 1))
-                           : lay.x_in_stage ? (lane + 32 * (grp ^ 1))
-                                            : (Lrow ^ 64);
-        const uint32_t x_off = 8 * kChunkBytes + (lay.p_in_stage ? 16 * 128 : 0);
-        float* v_slot = reinterpret_cast<float*>(smem + lay.off_m);  // [128] row max / row sum
+        float* v_slot = reinterpret_cast<float*>(smem + lay.off_v);  // [128] row max / row sum
         uint32_t gblk = 0, item = 0;
         bool alive = true;
         for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
@@ -485,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = (req == part.begin_req) ? part.begin_split : first_piece;
             const bool has_blocks = b1 > b0;
             if (has_blocks) {
-                // Q tile of this request: from its ring stage into the rails.
+                // Q tile of this request, from its ring stage: dims 0..447 into
+                // this lane's TMEM copy, dims 448..575 into the packed chunks
+                // (by the lane group 0 threads; both groups hold the same rows).
                 const uint32_t nq = gblk + item;
                 const uint32_t stq = nq % n_stages;
                 if (!named_bar_and(pair_bar, 64,
@@ -496,10 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* sq = sKV + stq * kStageBytes;
                 const bool have = r < p.q_box_rows;
 #pragma unroll 1
-                for (int k = 0; k < 5; ++k) {
-                    const int c = grp == 0 ? 2 * k : (k < 4 ? 2 * k + 1 : 8);
+                for (int c = 0; c < kTmemChunks; ++c) {
                     uint32_t w[32];
-                    if (have && !(grp == 0 && k == 4)) {
+                    if (have) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             ld_shared_v4(smem_u32(sq + c * kChunkBytes + sw128_offset(r, u)),
@@ -508,8 +470,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) w[i] = 0u;
                     }
-                    tmem_st32(tl + kColQ + 32 * k, w);
+                    tmem_st32(tl + kColQ + 32 * c, w);
                 }
+                if (half == 0 && r < static_cast<int>(lay.q_rows)) {
+                    // rows keep their 128-byte swizzle: both bases are 1024-aligned
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                sq + (kTmemChunks + i) * kChunkBytes + r * 128 + u * 16);
+                            *reinterpret_cast<uint4*>(sQr + i * lay.q_rows * 128 + r * 128 + u * 16) =
+                                v;
+                        }
+                }
+                fence_proxy_async_smem();
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&bars->q_ready);
@@ -524,52 +499,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t own[64];
-                tmem_ld32(tl + kColS, *reinterpret_cast<uint32_t(*)[32]>(own));
-                tmem_ld32(tl + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(own + 32));
+                uint32_t sv[32];
+                tmem_ld32(tl + kColS, sv);
                 tmem_ld_wait();
                 tc_fence_before();
-                if (!MLA_RAIL_LATE_SEMPTY) warp_arrive(&bars->s_empty);
+                warp_arrive(&bars->s_empty);
 
-                // Swap rail partials with the thread holding the other rail of
-                // this row: rail 0 keeps tokens 0..31, rail 1 tokens 32..63.
-                // (Padding rows skip it; their partner is padding too.)
-                const uint32_t x_base =
-                    lay.x_in_stage ? smem_u32(stage + x_off) : smem_u32(smem + lay.off_x);
-                const uint32_t send = x_base + x_slot * 128, recv = x_base + x_peer * 128;
-                // the tokens the partner keeps: rail 0 gives 32..63, rail 1 gives 0..31
-                const bool g0 = grp == 0;
-#pragma unroll
-                for (int k = 0; k < 8 && row_valid; ++k) {
-                    const uint32_t u = (k ^ (lane & 7)) * 16;
-                    st_shared_v4(send + u, g0 ? own[32 + 4 * k] : own[4 * k],
-                                 g0 ? own[33 + 4 * k] : own[4 * k + 1],
-                                 g0 ? own[34 + 4 * k] : own[4 * k + 2],
-                                 g0 ? own[35 + 4 * k] : own[4 * k + 3]);
-                }
-                named_bar_sync(pair_bar, 64);
-                uint32_t other[32];
-                if (row_valid) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t u = (k ^ (lane & 7)) * 16;
-                        ld_shared_v4(recv + u, other[4 * k], other[4 * k + 1], other[4 * k + 2],
-                                     other[4 * k + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) other[k] = 0u;
-                }
-                if (MLA_RAIL_LATE_SEMPTY) warp_arrive(&bars->s_empty);
-                const int keep = grp == 0 ? 0 : 32;
-                const int t0 = blk * kPage + keep;
+                const int t0 = blk * kPage + 32 * half;
                 float x[32];
                 float hmax = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float r0 = __uint_as_float(grp == 0 ? own[c] : other[c]);
-                    const float r1 = __uint_as_float(grp == 0 ? other[c] : own[32 + c]);
-                    x[c] = (row_valid && t0 + c < lim) ? (r0 + r1) * p.scale_log2 : -INFINITY;
+                    x[c] = (row_valid && t0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2
+                                                       : -INFINITY;
                     hmax = fmaxf(hmax, x[c]);
                 }
                 // Row max over both halves (the slot is rewritten only after
@@ -597,14 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_part += psum;
 
-                // O is rescaled after PV(g - 1), and a single P buffer is
-                // rewritten after PV(g - 1) too.  Per-stage P needs neither,
-                // but PV may trail by at most two pages: the parity waits on
-                // the two p_full / pv_done barriers stay unambiguous.  (The
-                // two warps of a pair see the same rows, hence the same
+                // O is rescaled after PV(g - 1).  P has a buffer per stage,
+                // but PV may trail by at most two pages so that the parity
+                // waits on the two p_full / pv_done barriers stay unambiguous.
+                // (The two warps of a pair see the same rows, hence the same
                 // rescale decision.)
                 const bool rescale = __any_sync(0xffffffffu, need && blk > b0);
-                const uint32_t lag = (rescale || !lay.p_in_stage) ? 1u : 2u;
+                const uint32_t lag = rescale ? 1u : 2u;
                 bool ok = true;
                 if (gblk >= lag) {
                     const uint32_t w = gblk - lag;
@@ -639,15 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(0, 0, 0, 0);
                     }
                 }
-                // (per-stage P holds rows 0..15 only; the swap slots follow)
-                uint8_t* pbuf = lay.p_in_stage ? stage + 8 * kChunkBytes : sP;
-                if (!lay.p_in_stage || r < 16) {
+                // P into the page's RoPE chunk (QK^T is done with it).
+                uint8_t* pbuf = stage + 8 * kChunkBytes;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t off = sw128_offset(r, 4 * grp + k);
-                        *reinterpret_cast<uint4*>(pbuf + off) =
-                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                    }
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t off = sw128_offset(r, 4 * half + k);
+                    *reinterpret_cast<uint4*>(pbuf + off) =
+                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -679,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     tmem_ld32(tl + kColO + 32 * cg, o);
                     tmem_ld_wait();
-                    const int dv0 = 256 * (cg >> 2) + 128 * grp + 32 * (cg & 3);
+                    const int dv0 = 256 * (cg >> 2) + 128 * half + 32 * (cg & 3);
                     if (!row_valid) continue;
                     if (split) {
                         float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
@@ -708,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++item;
             } else if (row_valid) {
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int dv0 = 256 * hh + 128 * grp;
+                    const int dv0 = 256 * hh + 128 * half;
                     if (split) {
                         float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
                         for (int v = 0; v < 32; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -719,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row_valid && grp == 0) {
+            if (row_valid && half == 0) {
                 if (split)
                     p.lseaccum[acc_row] = lse2;
                 else
@@ -737,13 +676,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-static cudaError_t rail_set_smem() {
+static cudaError_t tq_set_smem() {
     static int configured_mask = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(__atomic_load_n(&configured_mask, __ATOMIC_RELAXED) & (1 << dev))) {
-        e = cudaFuncSetAttribute(decode_rail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_tq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemMax));
         if (e != cudaSuccess) return e;
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
@@ -751,21 +690,21 @@ static cudaError_t rail_set_smem() {
     return cudaSuccess;
 }
 
-cudaError_t launch_decode_rail(const DecodeParams& p, const CUtensorMap& q_map,
-                               const CUtensorMap& kv_map, cudaStream_t stream) {
-    cudaError_t e = rail_set_smem();
+cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
+                             const CUtensorMap& kv_map, cudaStream_t stream) {
+    cudaError_t e = tq_set_smem();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_mtiles, p.num_parts, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = rail_layout(p.q_box_rows).bytes;
+    cfg.dynamicSmemBytes = tq_layout(p.q_box_rows).bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_rail_kernel, p, q_map, kv_map);
+    return cudaLaunchKernelEx(&cfg, decode_tq_kernel, p, q_map, kv_map);
 }
 
 }  // namespace mla

@@ -81,8 +81,8 @@ cudaError_t launch_sched(const int32_t* seqlens, int batch, int R, int num_parts
                          cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);
-cudaError_t launch_decode_rail(const DecodeParams& p, const CUtensorMap& q_map,
-                               const CUtensorMap& kv_map, cudaStream_t stream);
+cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
+                             const CUtensorMap& kv_map, cudaStream_t stream);
 cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map,
                                const CUtensorMap& kv_map, cudaStream_t stream);
 int pair_max_active_clusters();  // on the current device; 0 when the query fails

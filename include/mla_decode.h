@@ -265,17 +265,20 @@ MLA_API int mla_set_fixed_overhead(int blocks);
 /*
  * mla_set_decode_kernel -- which decode kernel mla_decode_fwd and
  * mla_decode_splitkv launch.  Process-wide; all compute the same function.
- *   MLA_KERNEL_SINGLE (default) one CTA per SM part and 64-row query tile,
+ *   MLA_KERNEL_AUTO   (default) MLA_KERNEL_TQ when s_q * h_q <= 32, else
+ *                     MLA_KERNEL_SINGLE (same split plan for both).
+ *   MLA_KERNEL_SINGLE one CTA per SM part and 64-row query tile,
  *                     Q in shared memory, two KV pages in flight.
  *   MLA_KERNEL_PAIR   one 2-CTA cluster per SM pair: the two CTAs split the
  *                     576 head dims, swap their partial QK^T scores through
  *                     distributed shared memory (the cluster exchange of
  *                     "[DeepSeek-3] FlashMLA", sec. 13) and each computes half
  *                     of the 512 output dims.
- *   MLA_KERNEL_RAIL   one CTA per SM part and query tile with Q in tensor
- *                     memory and QK^T as the two-rail weight-stationary GEMM
- *                     of "Blackwell 多轨矩乘(multi-rail GEMM)", sec. 2; up to
- *                     three KV pages in flight.
+ *   MLA_KERNEL_TQ     one CTA per SM part and query tile with Q's dims
+ *                     0..447 in tensor memory (the A operand of QK^T, as in
+ *                     "Blackwell 多轨矩乘(multi-rail GEMM)", sec. 1), so that
+ *                     three KV pages fit in shared memory for tiles of at
+ *                     most 32 query rows (two otherwise).
  * The split plan depends on the kernel (its number of SM parts), so metadata
  * must be rebuilt after a switch; a decode call with metadata built for a
  * kernel with another part count records MLA_ERR_METADATA_MISMATCH on the
@@ -284,7 +287,8 @@ MLA_API int mla_set_fixed_overhead(int blocks);
  */
 #define MLA_KERNEL_PAIR 0
 #define MLA_KERNEL_SINGLE 1
-#define MLA_KERNEL_RAIL 2
+#define MLA_KERNEL_TQ 2
+#define MLA_KERNEL_AUTO 3
 MLA_API int mla_set_decode_kernel(int kind);
 MLA_API int mla_get_decode_kernel(void);
 

@@ -38,7 +38,7 @@ def kernel_kind(request):
     api.set_decode_kernel(default)
 
 
-@pytest.mark.parametrize("kernel_kind", [0, 1, 2], indirect=True, ids=["pair", "single", "rail"])
+@pytest.mark.parametrize("kernel_kind", [0, 1, 2], indirect=True, ids=["pair", "single", "tq"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_kernel_parity(kernel_kind, case):
     b, s_q, h_q, seqlens, causal = case
@@ -80,7 +80,7 @@ def test_kernels_agree_and_switch_needs_new_metadata():
                                   w.causal, meta_pair, ns_pair, ws, out, lse)
             call.splitkv()
             assert api.mla_last_device_error() == _lib.MLA_ERR_METADATA_MISMATCH
-        api.set_decode_kernel(api.KERNEL_RAIL)
+        api.set_decode_kernel(api.KERNEL_TQ)
         meta_r, ns_r = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
         o_r, l_r = api.mla_decode_fwd(g.q, g.k_cache, g.block_table, g.cache_seqlens,
                                       w.softmax_scale, w.causal, meta_r, ns_r)
