@@ -102,10 +102,10 @@ __host__ __device__ constexpr TqLayout tq_layout(int q_box_rows) {
     l.bytes = l.off_misc + 64u;
     return l;
 }
+static_assert(tq_layout(32).n_stages == 3 && tq_layout(64).n_stages == 2, "stage counts");
 static_assert(tq_layout(16).bytes <= kSmemMax && tq_layout(32).bytes <= kSmemMax &&
                   tq_layout(64).bytes <= kSmemMax,
               "exceeds the 227 KB per-CTA shared memory limit");
-static_assert(tq_layout(32).n_stages == 3 && tq_layout(64).n_stages == 2, "stage counts");
 static_assert(kSmemMax < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
 
 struct Part {
@@ -292,18 +292,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
         Cursor ld = cursor_begin(p, part), ahead = ld;
+        uint32_t n_issued = 0;  // ring entries issued
+        // The first request's Q tile (ring entry 0) needs no block-table entry:
+        // it goes out before the look-ahead loads.
+        if (ld.valid) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->kv_full[0], q_bytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(&q_map, &bars->kv_full[0], sKV + c * kChunkBytes, 64 * c,
+                                mtile * kTileM, ld.req, policy);
+            }
+            __syncwarp();
+            n_issued = 1;
+        }
         int bid = 0;
         for (int i = 0; i < 32 && ahead.valid; ++i) {
             if (lane == static_cast<int>(ahead.g & 31))
                 bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
             cursor_next(p, part, ahead);
         }
-        uint32_t n_issued = 0;  // ring entries issued
         bool stop = false;
         while (ld.valid && !stop) {
             const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
-            // First block of a request: its Q tile goes into the ring first.
-            for (int entry = (ld.blk == ld.b0) ? 0 : 1; entry < 2; ++entry) {
+            // First block of a request: its Q tile goes into the ring first
+            // (already out for the part's first request).
+            for (int entry = (ld.blk == ld.b0 && ld.g > 0) ? 0 : 1; entry < 2; ++entry) {
                 const uint32_t n = ld.ring() - 1 + entry;
                 const uint32_t st = n % n_stages;
                 if (n >= n_stages && !warp_wait(&bars->kv_empty[st], ((n / n_stages) + 1) & 1, wc)) {
