@@ -4,7 +4,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
 Python binding) never imports, links or calls it, and shares no code with it.
 
-The C sources (``mla_oracle.c``, ``plan_oracle.c``) hold the arithmetic and
+The C sources (``mla_oracle.c``, ``sparse_oracle.c``, ``plan_oracle.c``) hold the arithmetic and
 cite the pages they follow; this module only compiles them with gcc and
 marshals numpy arrays through ctypes.
 
@@ -22,7 +22,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
-_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "plan_oracle.c")]
+_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "sparse_oracle.c"),
+         os.path.join(_HERE, "plan_oracle.c")]
 _lock = threading.Lock()
 _lib = None
 
@@ -63,6 +64,11 @@ def _load():
             lib.oracle_merge_pair.restype = None
             lib.oracle_lse_combine.argtypes = [I, P, P, I, P, P]
             lib.oracle_lse_combine.restype = None
+            lib.oracle_mla_sparse.argtypes = [P, P, P, I, I, I, I, I, I, I64, D, P, P, I]
+            lib.oracle_mla_sparse.restype = I
+            lib.oracle_mla_sparse_rows.argtypes = [P, P, P, I, I, I, I, I, I, I64, D, P, I64, P,
+                                                   P, I]
+            lib.oracle_mla_sparse_rows.restype = I
             lib.oracle_plan.argtypes = [P, I, I, I, I, P, P]
             lib.oracle_plan.restype = I
             _lib = lib
@@ -192,3 +198,56 @@ def plan(seqlens, num_parts: int, fixed_overhead: int, page: int = 64):
     if st != 0:
         raise RuntimeError(f"oracle_plan failed: {st}")
     return parts, ns
+
+
+class SparseProblem:
+    """One sparse decode problem in the oracle's layout.
+
+    q       : uint16 [b, s_q, h_q, d]           (bf16 bits)
+    kv      : uint16 [num_pages, page, d] or [num_pages, page, 1, d]
+    indices : int32 [b, s_q, topk]  physical token = page_id * page + offset,
+              < 0 for padding
+    """
+
+    def __init__(self, q, kv, indices, scale):
+        self.q = np.ascontiguousarray(q, dtype=np.uint16)
+        kv = np.asarray(kv, dtype=np.uint16)
+        if kv.ndim == 4:
+            assert kv.shape[2] == 1
+            kv = kv.reshape(kv.shape[0], kv.shape[1], kv.shape[3])
+        self.kv = np.ascontiguousarray(kv)
+        self.indices = np.ascontiguousarray(indices, dtype=np.int32)
+        self.b, self.s_q, self.h_q, self.d = self.q.shape
+        assert self.indices.shape[:2] == (self.b, self.s_q)
+        self.topk = self.indices.shape[2]
+        self.num_tokens = self.kv.shape[0] * self.kv.shape[1]
+        self.scale = float(scale)
+
+    def _args(self, dv):
+        return (_ptr(self.q), _ptr(self.kv), _ptr(self.indices), self.b, self.s_q, self.h_q,
+                self.topk, self.d, dv, self.num_tokens, self.scale)
+
+
+def mla_sparse(p: SparseProblem, dv: int = 512, nthreads: int = 1, allow_bad_index=False):
+    """Sparse decode: (out [b, s_q, h_q, dv], lse [b, h_q, s_q]) in fp64."""
+    lib = _load()
+    out = np.zeros((p.b, p.s_q, p.h_q, dv), dtype=np.float64)
+    lse = np.zeros((p.b, p.h_q, p.s_q), dtype=np.float64)
+    st = lib.oracle_mla_sparse(*p._args(dv), _ptr(out), _ptr(lse), int(nthreads))
+    if st != 0 and not (st == -5 and allow_bad_index):
+        raise RuntimeError(f"oracle_mla_sparse failed: {st}")
+    return out, lse
+
+
+def mla_sparse_rows(p: SparseProblem, units, dv: int = 512, nthreads: int = 1):
+    """Selected rows (request, row = s*h_q + h) of a sparse decode, fp64."""
+    lib = _load()
+    units = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+    n = units.shape[0]
+    out = np.zeros((n, dv), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    st = lib.oracle_mla_sparse_rows(*p._args(dv), _ptr(units), n, _ptr(out), _ptr(lse),
+                                    int(nthreads))
+    if st != 0:
+        raise RuntimeError(f"oracle_mla_sparse_rows failed: {st}")
+    return out, lse
