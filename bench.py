@@ -286,6 +286,23 @@ def measure_workload(w, torch, api, W_mod, K, Wup, dist=None):
     return res, (g, call)
 
 
+def measure_sparse(w, torch, api, W_mod, K, Wup):
+    """Sparse decode (per-token key lists): mla_decode_sparse_fwd steps in a
+    CUDA graph; the plan is built once, outside the timed steps."""
+    g = w.to("cuda")
+    meta, ns = api.mla_get_metadata_sparse(w.topk, w.b, w.h_q, w.s_q)
+    call = api.SparseDecodeCall(g.q, g.k_cache, g.indices, w.softmax_scale, meta, ns)
+    gr = capture(torch, call.fwd)
+    assert api.mla_last_device_error() == 0
+    ms_total, _ = time_steps(torch, gr, K, Wup)
+    code = api.mla_last_device_error()
+    assert code == 0, f"device error {code}"
+    res = {"ms_per_step": ms_total / K, "flops": W_mod.sparse_flops(w.indices, w.h_q),
+           "bytes": W_mod.sparse_hbm_bytes(w.indices, w.h_q), "pieces": int(ns[-1].item())}
+    del gr, call, g
+    return res
+
+
 def e2e_measure(w, torch, api, steps):
     """Public API from pinned host buffers, copies inside the timed region."""
     host = {
@@ -503,6 +520,19 @@ def main():
             }
             del gx, cx
             torch.cuda.empty_cache()
+        ws = W_mod.sparse()
+        kx = max(50, min(args.steps, 1000))
+        r = measure_sparse(ws, torch, api, W_mod, kx, 5)
+        t_s = r["ms_per_step"] * 1e-3
+        extra["sparse"] = {
+            "workload": ws.name, "ms_per_step": r["ms_per_step"],
+            "step_tflops": r["flops"] / t_s / 1e12, "step_gbs": r["bytes"] / t_s / 1e9,
+            "frac_bf16_peak": r["flops"] / t_s / 1e12 / bf16_peak,
+            "frac_hbm_peak": r["bytes"] / t_s / 1e9 / hbm_peak,
+            "pieces": r["pieces"], "steps": kx,
+        }
+        del ws
+        torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

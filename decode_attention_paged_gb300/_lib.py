@@ -23,6 +23,7 @@ MLA_ERR_METADATA_MISMATCH = -6
 MLA_ERR_NO_DEVICE = -7
 MLA_ERR_SEQ_TOO_LONG = -8
 MLA_ERR_BAD_ALIGNMENT = -9
+MLA_ERR_BAD_INDEX = -10
 
 # Every symbol include/mla_decode.h declares, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -43,6 +44,11 @@ SIGNATURES = {
     "mla_decode_combine": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _P, _I64, _I64, _I64, _P, _P]),
     "mla_decode_fwd_noalloc": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I,
                                     _I, _I, _F, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
+    "mla_metadata_size_sparse": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "mla_get_metadata_sparse": (_I, [_I, _I, _I, _I, _I, _P, _P, _P]),
+    "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+    "mla_decode_sparse_fwd": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I, _I, _I, _I, _I, _F,
+                                   _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P, _P]),
     "mla_last_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "mla_set_wait_budget_ns": (_I, [ctypes.c_uint64]),
     "mla_set_fixed_overhead": (_I, [_I]),

@@ -163,6 +163,99 @@ def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: 
     return out, lse
 
 
+def metadata_size_sparse(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> Tuple[int, int]:
+    mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    _lib.check(_lib.load().mla_metadata_size_sparse(batch, h_q, s_q, h_kv, ctypes.byref(mb),
+                                                    ctypes.byref(sb)), "mla_metadata_size_sparse")
+    return mb.value, sb.value
+
+
+def workspace_size_sparse(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> int:
+    b = ctypes.c_size_t()
+    _lib.check(_lib.load().mla_workspace_size_sparse(batch, h_q, s_q, h_kv, ctypes.byref(b)),
+               "mla_workspace_size_sparse")
+    return b.value
+
+
+def mla_get_metadata_sparse(topk: int, batch: int, h_q: int, s_q: int, h_kv: int = 1,
+                            device=None, stream: Optional[torch.cuda.Stream] = None,
+                            meta: Optional[torch.Tensor] = None,
+                            num_splits: Optional[torch.Tensor] = None):
+    """Split plan for sparse decode: every (request, query token) pair attends
+    to a list of `topk` selected positions.  Returns (meta, num_splits
+    int32 [batch * s_q + 1])."""
+    dev = torch.device(device) if device is not None else torch.device("cuda",
+                                                                      torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        mb, sb = metadata_size_sparse(batch, h_q, s_q, h_kv)
+        if meta is None:
+            meta = torch.empty(mb // 4, dtype=torch.int32, device=dev)
+        if num_splits is None:
+            num_splits = torch.empty(sb // 4, dtype=torch.int32, device=dev)
+        assert meta.dtype == torch.int32 and meta.numel() * 4 >= mb and meta.is_contiguous()
+        assert num_splits.dtype == torch.int32 and num_splits.numel() * 4 >= sb
+        _lib.check(_lib.load().mla_get_metadata_sparse(int(topk), batch, h_q, s_q, h_kv,
+                                                       _ptr(meta), _ptr(num_splits),
+                                                       _stream_ptr(stream)),
+                   "mla_get_metadata_sparse")
+    return meta, num_splits
+
+
+class SparseDecodeCall:
+    """Marshalled arguments of one sparse decode call (see include/mla_decode.h,
+    mla_decode_sparse_fwd): q [b, s_q, h_q, 576], k_cache [pages, 64, 1, 576]
+    with packed pages, indices int32 [b, s_q, topk] of positions page * 64 +
+    offset (< 0: padding)."""
+
+    def __init__(self, q, k_cache, indices, softmax_scale, meta, num_splits, workspace=None,
+                 out=None, lse=None, stream=None):
+        assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+        assert indices.dtype == torch.int32 and indices.is_contiguous()
+        b, s_q, h_q, d = q.shape
+        assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
+            q.stride(1) == h_q * D_QK
+        num_pages, page, h_kv, dk = k_cache.shape
+        assert dk == D_QK and k_cache.stride(3) == 1
+        assert tuple(indices.shape[:2]) == (b, s_q)
+        topk = indices.shape[2]
+        dev = q.device
+        with torch.cuda.device(dev):
+            if out is None:
+                out = torch.empty(b, s_q, h_q, D_V, dtype=torch.bfloat16, device=dev)
+            if lse is None:
+                lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
+            assert out.stride(3) == 1 and lse.is_contiguous()
+            if workspace is None:
+                workspace = torch.empty(workspace_size_sparse(b, h_q, s_q, h_kv),
+                                        dtype=torch.uint8, device=dev)
+        self.device = dev
+        self.out, self.lse, self.workspace = out, lse, workspace
+        self._keep = (q, k_cache, indices, meta, num_splits)
+        self.stream = stream
+        self.args = (
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
+            page, _ptr(indices), topk, b, s_q, h_q, h_kv, float(softmax_scale), _ptr(meta),
+            _ptr(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(out), out.stride(0), out.stride(1), out.stride(2), _ptr(lse))
+
+    def fwd(self):
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.load().mla_decode_sparse_fwd(*self.args, _stream_ptr(self.stream)),
+                       "mla_decode_sparse_fwd")
+        return self.out, self.lse
+
+
+def mla_decode_sparse_fwd(q: torch.Tensor, k_cache: torch.Tensor, indices: torch.Tensor,
+                          softmax_scale: float, meta: torch.Tensor, num_splits: torch.Tensor,
+                          workspace: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None):
+    """Sparse decode: out [b, s_q, h_q, 512] bf16 and lse [b, h_q, s_q] fp32 over
+    the positions listed in indices [b, s_q, topk]."""
+    return SparseDecodeCall(q, k_cache, indices, softmax_scale, meta, num_splits, workspace, out,
+                            lse, stream).fwd()
+
+
 def mla_last_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronise the stream and read/clear the device error word."""
     code = ctypes.c_int()

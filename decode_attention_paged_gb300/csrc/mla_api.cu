@@ -3,6 +3,7 @@
 // kernel launches.  The library owns no device memory of its own apart from the
 // per-device error word below (a module global, not an allocation).
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -83,10 +84,26 @@ int num_parts_of(int R, const DeviceInfo* d) {
     return parts > 0 ? parts : 1;
 }
 
+// Sparse decode always runs on the single-CTA kernel.
+int num_parts_single(int R, const DeviceInfo* d) {
+    const int parts = d->sms / n_mtiles_of(R);
+    return parts > 0 ? parts : 1;
+}
+
 int check_shape(int batch, int h_q, int s_q, int h_kv) {
     if (batch < 1 || h_q < 1 || s_q < 1) return MLA_ERR_INVALID_ARGUMENT;
     if (batch > sched_max_batch()) return MLA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(s_q) * h_q > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+// Sparse decode folds (request, query token) into the kernel's requests, each
+// with the h_q rows of one token.
+int check_shape_sparse(int batch, int h_q, int s_q, int h_kv, int topk) {
+    if (batch < 1 || h_q < 1 || s_q < 1 || topk < 0) return MLA_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(batch) * s_q > sched_max_batch()) return MLA_ERR_UNSUPPORTED;
+    if (h_q > (1 << 24) || topk > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
     return MLA_OK;
 }
@@ -102,8 +119,8 @@ void workspace_layout(int batch, int R, int parts, size_t* o_bytes, size_t* tota
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1) {
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool load_encode() {
     std::call_once(g_encode_once, [] {
         cudaDriverEntryPointQueryResult q;
         g_encode_status = cudaGetDriverEntryPointByVersion(
@@ -112,12 +129,32 @@ int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint
         if (g_encode_status == cudaSuccess && q != cudaDriverEntryPointSuccess)
             g_encode_status = cudaErrorNotSupported;
     });
-    if (g_encode_status != cudaSuccess || g_encode == nullptr) return MLA_ERR_CUDA;
+    return g_encode_status == cudaSuccess && g_encode != nullptr;
+}
+
+int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1) {
+    if (!load_encode()) return MLA_ERR_CUDA;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
     cuuint32_t box[3] = {64, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARGUMENT;
+}
+
+// 2-D row map of the whole cache for the sparse gather: [num_tokens x 576],
+// box {64, 1} (one row per gathered token, four rows per copy).
+int encode_rows_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
+    if (!load_encode()) return MLA_ERR_CUDA;
+    cuuint64_t dims[2] = {kDqk, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -143,6 +180,7 @@ const char* mla_strerror(int code) {
         case MLA_ERR_NO_DEVICE: return "no CUDA device";
         case MLA_ERR_SEQ_TOO_LONG: return "sequence longer than its block-table row";
         case MLA_ERR_BAD_ALIGNMENT: return "pointer or stride breaks the 16-byte alignment rule";
+        case MLA_ERR_BAD_INDEX: return "a sparse key index points past the end of the cache";
         default: return "unknown error";
     }
 }
@@ -193,7 +231,7 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
     const int parts = num_parts_of(R, d);
-    cudaError_t e = launch_sched(cache_seqlens_dev, batch, R, parts, n_mtiles_of(R),
+    cudaError_t e = launch_sched(cache_seqlens_dev, -1, batch, R, parts, n_mtiles_of(R),
                                  g_fixed_overhead.load(), static_cast<int32_t*>(meta_dev),
                                  num_splits_dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -215,6 +253,11 @@ int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
 
 namespace {
 
+int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                 size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
+                 void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream);
+
 int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int s_q, int h_q, int h_kv, void* out_dev,
                  int64_t out_batch_stride, int64_t out_s_stride, int64_t out_h_stride,
@@ -231,8 +274,19 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
+    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R,
+                        num_parts_of(R, d), s_q, h_q, 0, out_dev, out_batch_stride, out_s_stride,
+                        out_h_stride, lse_dev, stream);
+}
+
+// The combine launch for a plan of `batch` kernel requests of R rows each;
+// fold > 0 for sparse decode (see DecodeParams::fold).
+int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                 size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
+                 void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
     size_t o_bytes = 0, ws_need = 0;
-    workspace_layout(batch, R, num_parts_of(R, d), &o_bytes, &ws_need);
+    workspace_layout(batch, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
     CombineParams c{};
@@ -249,6 +303,7 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
     c.s_q = s_q;
     c.h_q = h_q;
     c.R = R;
+    c.fold = fold;
     cudaError_t e = launch_combine(c, reinterpret_cast<cudaStream_t>(stream), /*pdl=*/true);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -381,6 +436,133 @@ int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cach
     return combine_only(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, s_q, h_q,
                         h_kv, out_dev, out_batch_stride, out_s_stride, out_h_stride, lse_dev,
                         stream);
+}
+
+int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
+                             size_t* num_splits_bytes) {
+    int st = check_shape_sparse(batch, h_q, s_q, h_kv, 0);
+    if (st) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int parts = num_parts_single(h_q, d);
+    if (meta_bytes)
+        *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
+    if (num_splits_bytes)
+        *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(batch) * s_q + 1);
+    return MLA_OK;
+}
+
+int mla_get_metadata_sparse(int topk, int batch, int h_q, int s_q, int h_kv, void* meta_dev,
+                            int32_t* num_splits_dev, mla_stream_t stream) {
+    int st = check_shape_sparse(batch, h_q, s_q, h_kv, topk);
+    if (st) return st;
+    if (!meta_dev || !num_splits_dev) return MLA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(meta_dev) & 15u) ||
+        (reinterpret_cast<uintptr_t>(num_splits_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    cudaError_t e = launch_sched(nullptr, topk, batch * s_q, h_q, num_parts_single(h_q, d),
+                                 n_mtiles_of(h_q), g_fixed_overhead.load(),
+                                 static_cast<int32_t*>(meta_dev), num_splits_dev,
+                                 reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_workspace_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
+    int st = check_shape_sparse(batch, h_q, s_q, h_kv, 0);
+    if (st) return st;
+    if (!bytes) return MLA_ERR_INVALID_ARGUMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    size_t ob = 0;
+    workspace_layout(batch * s_q, h_q, num_parts_single(h_q, d), &ob, bytes);
+    return MLA_OK;
+}
+
+int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                          int64_t k_page_stride, int64_t k_token_stride, int num_pages,
+                          int page_size, const int32_t* indices_dev, int topk, int batch, int s_q,
+                          int h_q, int h_kv, float softmax_scale, const void* meta_dev,
+                          const int32_t* num_splits_dev, void* workspace_dev,
+                          size_t workspace_bytes, void* out_dev, int64_t out_batch_stride,
+                          int64_t out_s_stride, int64_t out_h_stride, float* lse_dev,
+                          mla_stream_t stream) {
+    int st = check_shape_sparse(batch, h_q, s_q, h_kv, topk);
+    if (st) return st;
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (!q_dev || !k_cache_dev || (!indices_dev && topk > 0) || !meta_dev || !num_splits_dev ||
+        !out_dev || !lse_dev)
+        return MLA_ERR_INVALID_ARGUMENT;
+    const int64_t q_tok = static_cast<int64_t>(h_q) * kDqk;  // one query token's rows
+    if (num_pages < 1 || static_cast<int64_t>(num_pages) * kPage > INT32_MAX ||
+        q_batch_stride < s_q * q_tok || k_token_stride < kDqk ||
+        k_page_stride < k_token_stride * kPage || out_h_stride < kDv ||
+        out_s_stride < out_h_stride * h_q || out_batch_stride < out_s_stride * s_q ||
+        !std::isfinite(softmax_scale))
+        return MLA_ERR_INVALID_ARGUMENT;
+    // The gather addresses the cache as one [num_pages * 64 x 576] row array,
+    // and the Q map walks the (request, query token) pairs with one stride.
+    if (k_page_stride != k_token_stride * kPage) return MLA_ERR_UNSUPPORTED;
+    if (batch > 1 && s_q > 1 && q_batch_stride != s_q * q_tok) return MLA_ERR_UNSUPPORTED;
+    if (!aligned16(q_dev) || !aligned16(k_cache_dev) || !aligned16(out_dev) ||
+        (q_batch_stride % 8) || (k_token_stride % 8) || (out_batch_stride % 8) ||
+        (out_s_stride % 8) || (out_h_stride % 8) ||
+        (reinterpret_cast<uintptr_t>(lse_dev) & 3u) ||
+        (reinterpret_cast<uintptr_t>(indices_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int nreq = batch * s_q, R = h_q;
+    const int parts = num_parts_single(R, d);
+    size_t o_bytes = 0, ws_need = 0;
+    workspace_layout(nreq, R, parts, &o_bytes, &ws_need);
+    if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
+
+    CUtensorMap q_map, kv_map;
+    const uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
+    const int64_t q_req_stride = s_q == 1 ? q_batch_stride : q_tok;
+    st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(nreq),
+                   kDqk * 2, static_cast<uint64_t>(q_req_stride) * 2, q_box_rows);
+    if (st) return st;
+    const int64_t num_tokens = static_cast<int64_t>(num_pages) * kPage;
+    st = encode_rows_2d(&kv_map, k_cache_dev, static_cast<uint64_t>(num_tokens),
+                        static_cast<uint64_t>(k_token_stride) * 2);
+    if (st) return st;
+
+    DecodeParams p{};
+    p.max_blocks = topk > 0 ? (topk + kPage - 1) / kPage : 1;
+    p.meta = static_cast<const int32_t*>(meta_dev);
+    p.num_splits = num_splits_dev;
+    p.out = static_cast<__nv_bfloat16*>(out_dev);
+    p.out_sb = out_batch_stride;
+    p.out_ss = out_s_stride;
+    p.out_sh = out_h_stride;
+    p.lse = lse_dev;
+    p.oaccum = static_cast<float*>(workspace_dev);
+    p.lseaccum = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + o_bytes);
+    p.batch = nreq;
+    p.s_q = s_q;
+    p.h_q = h_q;
+    p.R = R;
+    p.n_mtiles = n_mtiles_of(R);
+    p.num_parts = parts;
+    p.q_box_rows = static_cast<int>(q_box_rows);
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.causal = 0;
+    p.error_word = d->error_word;
+    p.budget_ns = g_budget_ns.load();
+    p.sparse = 1;
+    p.indices = indices_dev;
+    p.topk = topk;
+    p.num_tokens = num_tokens;
+    p.fold = s_q;
+    cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, nreq, R, parts,
+                        s_q, h_q, s_q, out_dev, out_batch_stride, out_s_stride, out_h_stride,
+                        lse_dev, stream);
 }
 
 int mla_last_device_error(mla_stream_t stream, int* code) {

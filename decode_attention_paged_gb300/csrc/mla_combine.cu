@@ -63,9 +63,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
-    const int s = row / p.h_q, h = row % p.h_q;
-    __nv_bfloat16* orow = p.out + req * p.out_sb + s * p.out_ss + h * p.out_sh + lane * 16;
-    float* lse_out = p.lse + (static_cast<int64_t>(req) * p.h_q + h) * p.s_q + s;
+    const OutMap om = out_map(req, row, p.h_q, p.s_q, p.fold, p.out_sb, p.out_ss, p.out_sh);
+    __nv_bfloat16* orow = p.out + om.out_off + lane * 16;
+    float* lse_out = p.lse + om.lse_idx;
     if (mx == -INFINITY) {
         uint4 z = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4*>(orow)[0] = z;

@@ -88,7 +88,7 @@ constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffBar = kOffP + kPBytes;
 constexpr uint32_t kOffXch = kOffBar + 256;            // uint2 [2][128]: pair exchange
-constexpr uint32_t kOffMisc = kOffXch + 2 * 128 * 8;    // tmem base, abort flag
+constexpr uint32_t kOffMisc = kOffXch + 2 * 128 * 8;    // tmem base, abort flag, key masks
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 static_assert(kChunks % 3 == 0, "QK^T is issued three chunks per turn");
@@ -106,7 +106,7 @@ __device__ __forceinline__ int blocks_of(int L) { return L > 0 ? (L + kPage - 1)
 // same list of work items.
 __device__ __forceinline__ void item_range(const DecodeParams& p, const Part& part, int req,
                                            int& L, int& nb, int& b0, int& b1) {
-    L = p.seqlens[req];
+    L = p.sparse ? p.topk : p.seqlens[req];
     if (L < 0) L = 0;
     nb = blocks_of(L);
     if (nb > p.max_blocks) nb = p.max_blocks;  // reported as MLA_ERR_SEQ_TOO_LONG
@@ -218,6 +218,16 @@ __device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& se
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bit j of b (j < 16) to bit 4 j.
+__device__ __forceinline__ uint64_t spread_4x(uint32_t b) {
+    uint64_t x = b & 0xffffu;
+    x = (x | (x << 24)) & 0x000000ff000000ffull;
+    x = (x | (x << 12)) & 0x000f000f000f000full;
+    x = (x | (x << 6)) & 0x0303030303030303ull;
+    x = (x | (x << 3)) & 0x1111111111111111ull;
+    return x;
+}
+
 // Chunks [C0, C0 + 3) of S = Q K^T for one page: 12 MMAs, each issued by one
 // elected lane of the converged warp, operand offsets known at compile time.
 template <int C0>
@@ -250,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint2* xch = reinterpret_cast<uint2*>(smem + kOffXch);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    // Sparse decode: bit t = stage row t holds a key (written before kv_full).
+    volatile uint64_t* key_mask = reinterpret_cast<volatile uint64_t*>(smem + kOffMisc + 8);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         part.begin_req = 0;
         part.end_req = -1;
     }
-    if (tid == 0) {
+    if (tid == 0 && !p.sparse) {
         for (int req = part.begin_req; req <= part.end_req; ++req) {
             const int L = p.seqlens[req];
             if (L > 0 && blocks_of(L) > p.max_blocks) raise_error(wc, MLA_ERR_SEQ_TOO_LONG);
@@ -334,23 +346,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         // waits and issues the copies); block-table entries are loaded 32
         // pages ahead, page g's by lane g % 32, and read with a shuffle when
         // page g is issued, so a load never waits for its page index.
+        //
+        // Sparse decode: a "page" is the next 64 entries of the request's key
+        // list.  Lane j < 16 gathers list entries j, j + 16, j + 32, j + 48
+        // into stage rows 4j .. 4j + 3 (nine row-gather copies, one per
+        // 64-dim chunk); the order of keys inside a page does not matter to
+        // the softmax.  Entries that are padding, past the list or outside
+        // the cache become row -1, which the copy fills with zeros, and lose
+        // their bit in the stage's key mask (published by lane 0 before its
+        // arrival on kv_full).
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
+        const bool sparse = p.sparse != 0;
         Cursor ld = cursor_begin(p, part), ahead = ld;
         int bid = 0;
-        for (int i = 0; i < 32 && ahead.valid; ++i) {
-            if (lane == static_cast<int>(ahead.g & 31))
-                bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+        int nxt[4] = {-1, -1, -1, -1};
+        auto load_rows = [&](const Cursor& c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = c.blk * kPage + (lane & 15) + 16 * k;
+                nxt[k] = (c.valid && lane < 16 && t < c.L)
+                             ? p.indices[static_cast<int64_t>(c.req) * p.topk + t]
+                             : -1;
+            }
+        };
+        if (sparse) {
+            load_rows(ahead);
             cursor_next(p, part, ahead);
+        } else {
+            for (int i = 0; i < 32 && ahead.valid; ++i) {
+                if (lane == static_cast<int>(ahead.g & 31))
+                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
+                cursor_next(p, part, ahead);
+            }
         }
         uint32_t n_kv = 0, n_q = 0;
         while (ld.valid) {
-            const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
             const int st = ld.g & 1;
+            int rows[4];
+            int page = 0;
+            if (sparse) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) rows[k] = nxt[k];
+                load_rows(ahead);  // the next page's entries, used one turn later
+            } else {
+                page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
+            }
             if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
-            if (lane == 0) {
+            uint8_t* dst = sKV + st * kStageBytes;
+            if (sparse) {
+                uint64_t mask = 0;
+                bool bad = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const bool v = rows[k] >= 0 && static_cast<int64_t>(rows[k]) < p.num_tokens;
+                    bad |= static_cast<int64_t>(rows[k]) >= p.num_tokens;
+                    if (!v) rows[k] = -1;
+                    mask |= spread_4x(__ballot_sync(0xffffffffu, v) & 0xffffu) << k;
+                }
+                if (bad) atomicCAS(p.error_word, 0, MLA_ERR_BAD_INDEX);
+                if (lane == 0) {
+                    key_mask[st] = mask;
+                    mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                }
+                __syncwarp();
+                if (lane < 16) {
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_gather4(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes + lane * 512,
+                                    64 * c, rows[0], rows[1], rows[2], rows[3], policy);
+                }
+            } else if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                uint8_t* dst = sKV + st * kStageBytes;
                 for (int c = 0; c < kChunks; ++c)
                     tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
                                 policy);
@@ -370,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
             if (ahead.valid) {
-                if (lane == static_cast<int>(ahead.g & 31))
+                if (!sparse && lane == static_cast<int>(ahead.g & 31))
                     bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
                 cursor_next(p, part, ahead);
             }
@@ -518,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = Lrow & 63, half = Lrow >> 6;
         const int row = mtile * kTileM + r;
         const bool row_valid = row < p.R;
-        const int s_idx = row / p.h_q, h_idx = row % p.h_q;
+        const int s_idx = row / p.h_q;  // query token (dense; causal limit)
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         uint32_t gblk = 0, n_items = 0, xseq = 0;
         bool alive = true;
@@ -547,12 +613,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bars->s_empty[st]);
 
-                const int t0 = blk * kPage + 32 * half;
+                // Keys of this thread's 32 columns: the first lim - t0 of
+                // them (dense), or the stage's key mask (sparse; the page's
+                // kv_full phase completed before its S, so the wait is a
+                // formality that orders the mask read).
+                uint32_t keys;
+                if (p.sparse) {
+                    if (!warp_wait(&bars->kv_full[st], (gblk >> 1) & 1, wc)) {
+                        alive = false;
+                        break;
+                    }
+                    keys = static_cast<uint32_t>(key_mask[st] >> (32 * half));
+                } else {
+                    const int n = lim - (blk * kPage + 32 * half);
+                    keys = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+                }
                 float x[32];
                 float hmax = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    x[c] = (t0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+                    x[c] = ((keys >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
                     hmax = fmaxf(hmax, x[c]);
                 }
                 float pmax;
@@ -602,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Last page of the sequence: zero the V rows past its length so
                 // stale slots (even NaN) cannot reach P.V through 0 * x.
-                if (blk == nb - 1 && (L & (kPage - 1)) != 0) {
+                // (Sparse pages: rows without a key were filled with zeros.)
+                if (!p.sparse && blk == nb - 1 && (L & (kPage - 1)) != 0) {
                     const int tail0 = L & (kPage - 1);
                     const int per_chunk = (kPage - tail0) * 8;  // 16-byte units
                     uint8_t* stage = sKV + st * kStageBytes;
@@ -644,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = empty ? 0.f : 1.f / l_tot;
             const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
             const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
+            const OutMap om = out_map(req, row, p.h_q, p.s_q, p.fold, p.out_sb, p.out_ss, p.out_sh);
             if (has_blocks) {
 #pragma unroll 1
                 for (int cg = 0; cg < 8; ++cg) {
@@ -661,8 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  __uint_as_float(o[4 * v + 2]) * inv,
                                                  __uint_as_float(o[4 * v + 3]) * inv);
                     } else {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            p.out + req * p.out_sb + s_idx * p.out_ss + h_idx * p.out_sh + dv0);
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + om.out_off + dv0);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             uint32_t w[4];
@@ -682,8 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv);
                     for (int v = 0; v < 64; ++v) dst[v * 2 + half] = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + req * p.out_sb + s_idx * p.out_ss +
-                                                          h_idx * p.out_sh);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + om.out_off);
                     for (int v = 0; v < 32; ++v) dst[v * 2 + half] = make_uint4(0, 0, 0, 0);
                 }
             }
@@ -691,8 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (split)
                     p.lseaccum[acc_row] = lse2;
                 else
-                    p.lse[(static_cast<int64_t>(req) * p.h_q + h_idx) * p.s_q + s_idx] =
-                        empty ? -INFINITY : lse2 * 0.69314718055994531f;
+                    p.lse[om.lse_idx] = empty ? -INFINITY : lse2 * 0.69314718055994531f;
             }
         }
     }

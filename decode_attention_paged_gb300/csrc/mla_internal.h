@@ -62,7 +62,39 @@ struct DecodeParams {
     int causal;
     int* error_word;
     uint64_t budget_ns;
+    // Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11): the kernel's requests
+    // are the (i, s) query tokens, each with its own key list of topk
+    // physical positions indices[(i * fold + s) * topk + k] (< 0: padding),
+    // gathered through a 2-D [num_tokens x 576] row map of the cache.
+    // sparse == 0: dense decode through block_table.  (indices may be null
+    // when topk == 0.)
+    int sparse;
+    const int32_t* indices;
+    int topk;
+    int64_t num_tokens;  // num_pages * 64: positions past it are reported
+    int fold;            // sparse: s_q of the caller (request r = i * fold + s); dense: 0
 };
+
+// Output address of (request r, row) for both layouts: dense rows are
+// s * h_q + h of request r; sparse requests fold (i, s) and rows are heads.
+struct OutMap {
+    int64_t out_off;   // element offset into out
+    int64_t lse_idx;   // element index into lse [b][h_q][s_q]
+};
+__device__ __forceinline__ OutMap out_map(int r, int row, int h_q, int s_q, int fold,
+                                          int64_t out_sb, int64_t out_ss, int64_t out_sh) {
+    OutMap m;
+    if (fold > 0) {
+        const int i = r / fold, s = r % fold;
+        m.out_off = i * out_sb + s * out_ss + row * out_sh;
+        m.lse_idx = (static_cast<int64_t>(i) * h_q + row) * fold + s;
+    } else {
+        const int s = row / h_q, h = row % h_q;
+        m.out_off = r * out_sb + s * out_ss + h * out_sh;
+        m.lse_idx = (static_cast<int64_t>(r) * h_q + h) * s_q + s;
+    }
+    return m;
+}
 
 struct CombineParams {
     const int32_t* meta;
@@ -73,11 +105,13 @@ struct CombineParams {
     int64_t out_sb, out_ss, out_sh;
     float* lse;
     int batch, s_q, h_q, R;
+    int fold;  // as DecodeParams::fold
 };
 
 // Host launchers (return a cudaError_t).
-cudaError_t launch_sched(const int32_t* seqlens, int batch, int R, int num_parts, int n_mtiles,
-                         int fixed_overhead, int32_t* meta, int32_t* num_splits,
+// seqlens == nullptr: every request has uniform_len keys.
+cudaError_t launch_sched(const int32_t* seqlens, int uniform_len, int batch, int R, int num_parts,
+                         int n_mtiles, int fixed_overhead, int32_t* meta, int32_t* num_splits,
                          cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);

@@ -124,6 +124,19 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* ba
         "l"(policy)
         : "memory");
 }
+// Row gather of a 2-D tensor map whose box is {cols, 1}: rows r0..r3 (any
+// order, out-of-range rows read as zeros) land as four consecutive box rows
+// at dst, with the map's swizzle.
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int col, int r0, int r1, int r2, int r3,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::"
+        "bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3), "l"(policy)
+        : "memory");
+}
 // Ask L2 to fetch one 3-D tile of a tensor map (no shared memory, no
 // completion tracking); a later TMA load of the same tile then hits L2.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1,

@@ -158,3 +158,93 @@ def hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int) -> int:
     """Algorithmic bytes: every cached token once (1152 B), q in, out and lse out."""
     rows = len(seqlens) * s_q * h_q
     return sum(int(L) for L in seqlens) * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)
+
+
+# ---------------------------------------------------------------- sparse decode
+# Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11): every query token attends
+# to its own list of topk cache positions, index = physical page * 64 + offset.
+# The selector that makes the lists is outside the path; here each list is
+# topk distinct tokens of the request's own context, drawn at random (seeded,
+# in random order), optionally with some slots turned into padding (-1).
+
+@dataclasses.dataclass
+class SparseWorkload:
+    name: str
+    q: torch.Tensor        # [b, s_q, h_q, 576] bf16
+    k_cache: torch.Tensor  # [num_pages, 64, 1, 576] bf16
+    indices: torch.Tensor  # [b, s_q, topk] int32
+    softmax_scale: float
+
+    @property
+    def b(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def s_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def h_q(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def topk(self) -> int:
+        return self.indices.shape[2]
+
+    @property
+    def num_tokens(self) -> int:
+        return self.k_cache.shape[0] * PAGE
+
+    def to(self, device) -> "SparseWorkload":
+        return dataclasses.replace(self, q=self.q.to(device), k_cache=self.k_cache.to(device),
+                                   indices=self.indices.to(device))
+
+
+def make_sparse(name: str, b: int, s_q: int, h_q: int, topk: int, context: int,
+                pad_frac: float = 0.0, extra_pages: int = 0, seed_offset: int = 0,
+                scale: float = SCALE) -> SparseWorkload:
+    """Request i owns `context` tokens on ceil(context / 64) pages of a random
+    permutation of the pool (seed 3); list (i, s) holds min(topk, context)
+    distinct tokens of that context in random order (seed 5), the rest of its
+    topk slots -1; then a fraction pad_frac of all slots is set to -1 (seed 6)."""
+    npg = (context + PAGE - 1) // PAGE
+    num_pages = b * npg + extra_pages
+    perm = torch.randperm(num_pages, generator=_gen(3 + seed_offset)).to(torch.int64)
+    bt = perm[: b * npg].view(b, npg)
+    g = _gen(5 + seed_offset)
+    k = min(topk, context)
+    idx = torch.full((b, s_q, topk), -1, dtype=torch.int64)
+    for i in range(b):
+        for s in range(s_q):
+            t = torch.randperm(context, generator=g)[:k]
+            idx[i, s, :k] = bt[i, t // PAGE] * PAGE + t % PAGE
+    if pad_frac > 0:
+        drop = torch.rand((b, s_q, topk), generator=_gen(6 + seed_offset)) < pad_frac
+        idx[drop] = -1
+    q = _randn_bf16((b, s_q, h_q, D_QK), 1 + seed_offset)
+    k_cache = _randn_bf16((num_pages, PAGE, 1, D_QK), 2 + seed_offset)
+    return SparseWorkload(name, q, k_cache, idx.to(torch.int32).contiguous(), scale)
+
+
+def sparse(seed_offset: int = 0) -> SparseWorkload:
+    """batch 128, s_q 2, h_q 128, topk 2048 of a 4096-token context per request."""
+    return make_sparse("sparse b128 s_q2 h_q128 topk2048 ctx4096", 128, 2, 128, 2048, 4096,
+                       seed_offset=seed_offset)
+
+
+def random_sparse_case(seed: int, b: int, s_q: int, h_q: int, topk: int, context: int,
+                       pad_frac: float = 0.0) -> SparseWorkload:
+    return make_sparse(f"sparse seed{seed}", b, s_q, h_q, topk, context, pad_frac,
+                       extra_pages=3, seed_offset=10 * seed)
+
+
+def sparse_flops(indices: torch.Tensor, h_q: int) -> int:
+    """Algorithmic FLOPs: 2*(576+512) per (query row, listed key); padding adds none."""
+    return int((indices >= 0).sum().item()) * h_q * 2 * (D_QK + D_V)
+
+
+def sparse_hbm_bytes(indices: torch.Tensor, h_q: int) -> int:
+    """Algorithmic bytes: each listed key row once per list (1152 B), q in, out and lse out."""
+    b, s_q, _ = indices.shape
+    rows = b * s_q * h_q
+    return int((indices >= 0).sum().item()) * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)

@@ -67,7 +67,8 @@ enum {
     MLA_ERR_METADATA_MISMATCH = -6,  /* device: metadata built for other shapes */
     MLA_ERR_NO_DEVICE = -7,          /* no CUDA device visible                  */
     MLA_ERR_SEQ_TOO_LONG = -8,       /* device: L_i > 64 * max_blocks_per_seq   */
-    MLA_ERR_BAD_ALIGNMENT = -9       /* a pointer/stride breaks 16-byte rules   */
+    MLA_ERR_BAD_ALIGNMENT = -9,      /* a pointer/stride breaks 16-byte rules   */
+    MLA_ERR_BAD_INDEX = -10          /* device: a sparse index past the cache   */
 };
 
 #define MLA_HEAD_DIM_QK 576
@@ -237,6 +238,59 @@ MLA_API int mla_decode_fwd_noalloc(const void *q_dev, int64_t q_batch_stride,
                                    const int32_t *num_splits_dev, void *out_dev,
                                    int64_t out_batch_stride, int64_t out_s_stride,
                                    int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
+
+/*
+ * Sparse decode -- attention over a per-query-token list of selected cache
+ * positions instead of a request's whole prefix.  Source: "[DeepSeek-3]
+ * FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐", sec. 11 (Sparse FlashMLA: an
+ * upper layer picks top-k tokens per query token and passes their physical
+ * positions, index = page_id * 64 + offset, so no block table is needed; the
+ * kernel gathers those rows and runs QK -> online softmax -> PV).
+ * For request i, query token s, head h, with keys
+ *     K(i, s) = [ indices[i][s][k] : 0 <= k < topk, 0 <= index < num_pages * 64 ]
+ *     x_k     = softmax_scale * dot(q[i][s][h][:], row(index_k)[0:576]),
+ *               row(n) = k_cache[n / 64][n % 64][0][:]
+ *     lse[i][h][s]    = ln sum_k exp(x_k)
+ *     out[i][s][h][:] = sum_k exp(x_k - lse) * row(index_k)[0:512]
+ * The page leaves these open; this library reads them as:
+ *   - an index < 0 is padding and adds no key;
+ *   - an index >= num_pages * 64 adds no key and is reported as
+ *     MLA_ERR_BAD_INDEX by mla_last_device_error (the call still completes);
+ *   - a position listed twice counts twice (the list is attended as given);
+ *   - no causal mask (the selector decides what each token may see);
+ *   - an empty key set gives out = 0 and lse = -inf.
+ *
+ * mla_metadata_size_sparse / mla_workspace_size_sparse: buffer sizes, as
+ *   mla_metadata_size / mla_workspace_size (num_splits is int32[batch*s_q + 1]).
+ * mla_get_metadata_sparse: the split plan for lists of `topk` entries (every
+ *   (i, s) pair is one unit of topk keys).  Enqueues one kernel on `stream`.
+ * mla_decode_sparse_fwd: arguments as mla_decode_fwd, with
+ *   indices_dev  int32 [batch][s_q][topk], contiguous, 4-byte aligned (may
+ *                be NULL when topk == 0);
+ *   q_dev        as mla_decode_fwd, and when batch > 1 and s_q > 1 also
+ *                q_batch_stride == s_q * h_q * 576 (else MLA_ERR_UNSUPPORTED);
+ *   k_cache_dev  as mla_decode_fwd, with the pages packed back to back:
+ *                k_page_stride == 64 * k_token_stride (else UNSUPPORTED),
+ *                num_pages * 64 < 2^31;
+ *   out_dev, lse_dev as mla_decode_fwd.
+ * Constraints: batch * s_q <= 16384, 0 <= topk <= 2^24, h_kv = 1.
+ * Enqueues the decode kernel and the combine kernel on `stream`;
+ * graph-capturable.
+ */
+MLA_API int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t *meta_bytes,
+                                     size_t *num_splits_bytes);
+MLA_API int mla_get_metadata_sparse(int topk, int batch, int h_q, int s_q, int h_kv,
+                                    void *meta_dev, int32_t *num_splits_dev, mla_stream_t stream);
+MLA_API int mla_workspace_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t *bytes);
+MLA_API int mla_decode_sparse_fwd(const void *q_dev, int64_t q_batch_stride,
+                                  const void *k_cache_dev, int64_t k_page_stride,
+                                  int64_t k_token_stride, int num_pages, int page_size,
+                                  const int32_t *indices_dev, int topk, int batch, int s_q,
+                                  int h_q, int h_kv, float softmax_scale, const void *meta_dev,
+                                  const int32_t *num_splits_dev, void *workspace_dev,
+                                  size_t workspace_bytes, void *out_dev, int64_t out_batch_stride,
+                                  int64_t out_s_stride, int64_t out_h_stride, float *lse_dev,
+                                  mla_stream_t stream);
 
 /*
  * mla_last_device_error -- synchronise `stream`, then read and clear the

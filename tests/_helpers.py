@@ -77,3 +77,21 @@ def gather_units(out, lse, units, h_q):
     go = np.stack([o[i, rho // h_q, rho % h_q] for i, rho in units])
     gl = np.array([l[i, rho % h_q, rho // h_q] for i, rho in units])
     return go, gl
+
+
+def sparse_problem(w) -> oracle.SparseProblem:
+    return oracle.SparseProblem(oracle.bf16_bits(w.q), oracle.bf16_bits(w.k_cache),
+                                w.indices.numpy(), w.softmax_scale)
+
+
+def run_gpu_sparse(w, expect_code: int = 0):
+    """Sparse decode of a SparseWorkload through the C ABI; checks the device
+    error word against expect_code."""
+    from decode_attention_paged_gb300 import api
+
+    g = w.to("cuda")
+    meta, ns = api.mla_get_metadata_sparse(w.topk, w.b, w.h_q, w.s_q)
+    out, lse = api.mla_decode_sparse_fwd(g.q, g.k_cache, g.indices, w.softmax_scale, meta, ns)
+    code = api.mla_last_device_error()
+    assert code == expect_code, f"device error code {code}, expected {expect_code}"
+    return out, lse

@@ -80,3 +80,45 @@ def test_without_gpu_calls_report_no_device(lib):
         pytest.skip("a GPU is present")
     mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.mla_metadata_size(4, 16, 1, 1, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_NO_DEVICE
+
+
+def test_sparse_host_side_argument_checks(lib):
+    E = _lib
+    mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.mla_metadata_size_sparse(0, 16, 1, 1, ctypes.byref(mb), ctypes.byref(sb)) == E.MLA_ERR_INVALID_ARGUMENT
+    assert lib.mla_metadata_size_sparse(1, 16, 1, 2, ctypes.byref(mb), ctypes.byref(sb)) == E.MLA_ERR_UNSUPPORTED
+    # batch * s_q is the scheduler's request count: at most 16384
+    assert lib.mla_metadata_size_sparse(16384, 16, 2, 1, ctypes.byref(mb), ctypes.byref(sb)) == E.MLA_ERR_UNSUPPORTED
+    assert lib.mla_get_metadata_sparse(-1, 1, 16, 1, 1, None, None, None) == E.MLA_ERR_INVALID_ARGUMENT
+    assert lib.mla_get_metadata_sparse(64, 1, 16, 1, 1, None, None, None) == E.MLA_ERR_INVALID_ARGUMENT
+    ws = ctypes.c_size_t()
+    assert lib.mla_workspace_size_sparse(1, 16, 1, 1, None) == E.MLA_ERR_INVALID_ARGUMENT
+
+    # Fake, never dereferenced, 256-byte aligned addresses: every check below
+    # happens on the host before the device is queried.
+    P = 1 << 20
+    D, DV = 576, 512
+
+    def call(**kw):
+        a = dict(q=P, qsb=16 * D, kc=P, kps=64 * D, kts=D, pages=4, page=64, idx=P, topk=64,
+                 b=1, s_q=1, h_q=16, h_kv=1, scale=1.0, meta=P, ns=P, ws=P, wsb=1 << 30, out=P,
+                 osb=16 * DV, oss=16 * DV, osh=DV, lse=P)
+        a.update(kw)
+        return lib.mla_decode_sparse_fwd(a["q"], a["qsb"], a["kc"], a["kps"], a["kts"], a["pages"],
+                                         a["page"], a["idx"], a["topk"], a["b"], a["s_q"], a["h_q"],
+                                         a["h_kv"], a["scale"], a["meta"], a["ns"], a["ws"],
+                                         a["wsb"], a["out"], a["osb"], a["oss"], a["osh"],
+                                         a["lse"], None)
+
+    assert call(page=32) == E.MLA_ERR_UNSUPPORTED
+    assert call(idx=None) == E.MLA_ERR_INVALID_ARGUMENT
+    assert call(topk=-1) == E.MLA_ERR_INVALID_ARGUMENT
+    assert call(kps=65 * D) == E.MLA_ERR_UNSUPPORTED          # pages not packed
+    assert call(b=2, s_q=2, qsb=2 * 16 * D + 8, oss=16 * DV, osb=2 * 16 * DV) == E.MLA_ERR_UNSUPPORTED
+    assert call(idx=P + 2) == E.MLA_ERR_BAD_ALIGNMENT
+    assert call(q=P + 8) == E.MLA_ERR_BAD_ALIGNMENT
+    assert call(scale=float("nan")) == E.MLA_ERR_INVALID_ARGUMENT
+    import torch
+
+    if not torch.cuda.is_available():
+        assert call() == E.MLA_ERR_NO_DEVICE
