@@ -146,21 +146,6 @@ int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint
     return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARGUMENT;
 }
 
-// 2-D row map of the whole cache for the sparse gather: [num_tokens x 576],
-// box {64, 1} (one row per gathered token, four rows per copy).
-int encode_rows_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes) {
-    if (!load_encode()) return MLA_ERR_CUDA;
-    cuuint64_t dims[2] = {kDqk, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARGUMENT;
-}
-
 }  // namespace
 }  // namespace mla
 
@@ -527,8 +512,10 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
                    kDqk * 2, static_cast<uint64_t>(q_req_stride) * 2, q_box_rows);
     if (st) return st;
     const int64_t num_tokens = static_cast<int64_t>(num_pages) * kPage;
-    st = encode_rows_2d(&kv_map, k_cache_dev, static_cast<uint64_t>(num_tokens),
-                        static_cast<uint64_t>(k_token_stride) * 2);
+    // (The page map is not read in sparse mode; the kernel takes one.)
+    st = encode_3d(&kv_map, k_cache_dev, kDqk, kPage, static_cast<uint64_t>(num_pages),
+                   static_cast<uint64_t>(k_token_stride) * 2,
+                   static_cast<uint64_t>(k_page_stride) * 2, kPage);
     if (st) return st;
 
     DecodeParams p{};
@@ -557,6 +544,8 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     p.indices = indices_dev;
     p.topk = topk;
     p.num_tokens = num_tokens;
+    p.kv_bytes = static_cast<const uint8_t*>(k_cache_dev);
+    p.kv_token_bytes = k_token_stride * 2;
     p.fold = s_q;
     cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;

@@ -29,7 +29,12 @@
 //   - Warp roles: warp 0 = TMA producer (lane 0 issues; the warp's lanes
 //     keep block-table entries loaded 32 pages ahead), warp 1 = TMEM owner
 //     and MMA issuer (converged warp, elect.sync), warps 2..5 = softmax /
-//     correction / epilogue (one thread per TMEM lane).
+//     correction / epilogue (one thread per TMEM lane), warps 6..9 = row
+//     gather for sparse decode (idle in dense decode).
+//   - Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11) gathers each key row
+//     with 16-byte cp.async copies, eight threads per row: measured on GB300
+//     at the rate of the tiled TMA page load, while row-gather TMA copies
+//     (four rows per instruction) reached under a quarter of it.
 //   - Q and each 64-token page are TMA-loaded as 9 chunks of [64 x 64] bf16
 //     with 128-byte swizzle; V is the first 8 chunks of the same page, read by
 //     the PV MMA as an MN-major operand, so the page is loaded once.
@@ -49,7 +54,8 @@ namespace mla {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kGatherWarp0 = 6;  // warps 6..9: sparse-decode row gather
 constexpr uint32_t kQBytes = kChunks * kChunkBytes;      // 73728
 constexpr uint32_t kStageBytes = kChunks * kChunkBytes;  // 73728
 constexpr uint32_t kPBytes = 64 * 128;                   // P [64 rows x 64 tokens] bf16
@@ -218,16 +224,6 @@ __device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& se
     return __all_sync(0xffffffffu, ok);
 }
 
-// Bit j of b (j < 16) to bit 4 j.
-__device__ __forceinline__ uint64_t spread_4x(uint32_t b) {
-    uint64_t x = b & 0xffffu;
-    x = (x | (x << 24)) & 0x000000ff000000ffull;
-    x = (x | (x << 12)) & 0x000f000f000f000full;
-    x = (x | (x << 6)) & 0x0303030303030303ull;
-    x = (x | (x << 3)) & 0x1111111111111111ull;
-    return x;
-}
-
 // Chunks [C0, C0 + 3) of S = Q K^T for one page: 12 MMAs, each issued by one
 // elected lane of the converged warp, operand offsets known at compile time.
 template <int C0>
@@ -260,15 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint2* xch = reinterpret_cast<uint2*>(smem + kOffXch);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-    // Sparse decode: bit t = stage row t holds a key (written before kv_full).
-    volatile uint64_t* key_mask = reinterpret_cast<volatile uint64_t*>(smem + kOffMisc + 8);
+    // Sparse decode: key_part[2 * stage + w] has bit t set when stage row t
+    // holds a key; the two gather warps of a stage own disjoint bits (written
+    // before their kv_full arrivals).
+    volatile uint64_t* key_part = reinterpret_cast<volatile uint64_t*>(smem + kOffMisc + 8);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_full[s], p.sparse ? 2 : 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
         mbar_init(&bars->q_full, 1);
@@ -347,33 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pages ahead, page g's by lane g % 32, and read with a shuffle when
         // page g is issued, so a load never waits for its page index.
         //
-        // Sparse decode: a "page" is the next 64 entries of the request's key
-        // list.  Lane j < 16 gathers list entries j, j + 16, j + 32, j + 48
-        // into stage rows 4j .. 4j + 3 (nine row-gather copies, one per
-        // 64-dim chunk); the order of keys inside a page does not matter to
-        // the softmax.  Entries that are padding, past the list or outside
-        // the cache become row -1, which the copy fills with zeros, and lose
-        // their bit in the stage's key mask (published by lane 0 before its
-        // arrival on kv_full).
+        // Sparse decode: the gather warps fill the KV ring; this warp only
+        // loads each request's Q tile.
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
         const bool sparse = p.sparse != 0;
         Cursor ld = cursor_begin(p, part), ahead = ld;
         int bid = 0;
-        int nxt[4] = {-1, -1, -1, -1};
-        auto load_rows = [&](const Cursor& c) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = c.blk * kPage + (lane & 15) + 16 * k;
-                nxt[k] = (c.valid && lane < 16 && t < c.L)
-                             ? p.indices[static_cast<int64_t>(c.req) * p.topk + t]
-                             : -1;
-            }
-        };
-        if (sparse) {
-            load_rows(ahead);
-            cursor_next(p, part, ahead);
-        } else {
+        if (!sparse) {
             for (int i = 0; i < 32 && ahead.valid; ++i) {
                 if (lane == static_cast<int>(ahead.g & 31))
                     bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
@@ -382,47 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t n_kv = 0, n_q = 0;
         while (ld.valid) {
-            const int st = ld.g & 1;
-            int rows[4];
-            int page = 0;
-            if (sparse) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) rows[k] = nxt[k];
-                load_rows(ahead);  // the next page's entries, used one turn later
-            } else {
-                page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
-            }
-            if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
-            uint8_t* dst = sKV + st * kStageBytes;
-            if (sparse) {
-                uint64_t mask = 0;
-                bool bad = false;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const bool v = rows[k] >= 0 && static_cast<int64_t>(rows[k]) < p.num_tokens;
-                    bad |= static_cast<int64_t>(rows[k]) >= p.num_tokens;
-                    if (!v) rows[k] = -1;
-                    mask |= spread_4x(__ballot_sync(0xffffffffu, v) & 0xffffu) << k;
-                }
-                if (bad) atomicCAS(p.error_word, 0, MLA_ERR_BAD_INDEX);
+            if (!sparse) {
+                const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
+                const int st = ld.g & 1;
+                if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
                 if (lane == 0) {
-                    key_mask[st] = mask;
                     mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                    uint8_t* dst = sKV + st * kStageBytes;
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0,
+                                    page, policy);
                 }
                 __syncwarp();
-                if (lane < 16) {
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_gather4(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes + lane * 512,
-                                    64 * c, rows[0], rows[1], rows[2], rows[3], policy);
-                }
-            } else if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0, page,
-                                policy);
+                ++n_kv;
             }
-            __syncwarp();
-            ++n_kv;
             if (ld.blk == ld.b0) {  // first block of a request: its Q tile
                 if (ld.item > 0 && !warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
                 if (lane == 0) {
@@ -435,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++n_q;
             }
             // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
-            if (ahead.valid) {
-                if (!sparse && lane == static_cast<int>(ahead.g & 31))
+            if (!sparse && ahead.valid) {
+                if (lane == static_cast<int>(ahead.g & 31))
                     bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
                 cursor_next(p, part, ahead);
             }
@@ -577,6 +529,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (leader) mbar_drain(&bars->drain, 0, kDrainBudgetNs);
         __syncwarp();
+    } else if (warp >= kGatherWarp0) {
+        // ------------------------------------------- sparse-decode row gather
+        // Warps 6, 7 fill the stage of even pages, warps 8, 9 that of odd
+        // pages, so two pages are in flight.  A page is the next 64 entries of
+        // the request's key list; eight threads copy one cache row (nine
+        // 128-byte lines, one 16-byte piece of each per thread) into the
+        // page's row of every 64-dim chunk, in the 128-byte-swizzled layout
+        // the MMAs read.  Entries that are padding, past the list or outside
+        // the cache fill their row with zeros and lose their bit in the key
+        // mask.  Each thread waits for its own copies and fences them for the
+        // tensor core before its warp arrives on kv_full.
+        if (p.sparse) {
+            const int gw = warp - kGatherWarp0;
+            const int grp = gw >> 1, wl = gw & 1;
+            const int tl = 32 * wl + lane;
+            const int uu = tl & 7, tb = tl >> 3;  // 16-byte piece; rows tb + 8 j
+            const int64_t tok_bytes = p.kv_token_bytes;
+            int cur[8], nxt[8];
+            auto load_rows = [&](int (&d)[8], const Cursor& c) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = c.blk * kPage + tb + 8 * j;
+                    d[j] = (c.valid && t < c.L) ? p.indices[static_cast<int64_t>(c.req) * p.topk + t]
+                                                : -1;
+                }
+            };
+            auto skip2 = [&](Cursor& c) {
+                if (c.valid) cursor_next(p, part, c);
+                if (c.valid) cursor_next(p, part, c);
+            };
+            Cursor c = cursor_begin(p, part);
+            if (grp == 1 && c.valid) cursor_next(p, part, c);
+            load_rows(cur, c);
+            while (c.valid) {
+                const int st = c.g & 1;  // == grp
+                Cursor n2 = c;
+                skip2(n2);
+                load_rows(nxt, n2);  // this group's next page, used one turn later
+                if (c.g >= 2 && !warp_wait(&bars->kv_empty[st], ((c.g >> 1) + 1) & 1, wc)) break;
+                uint8_t* stage = sKV + st * kStageBytes;
+                uint64_t mask = 0;
+                bool bad = false;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int ix = cur[j];
+                    const bool v = ix >= 0 && static_cast<int64_t>(ix) < p.num_tokens;
+                    bad |= static_cast<int64_t>(ix) >= p.num_tokens;
+                    const uint8_t* src =
+                        p.kv_bytes + (v ? static_cast<int64_t>(ix) * tok_bytes : 0) + uu * 16;
+                    const uint32_t dst = smem_u32(stage + sw128_offset(tb + 8 * j, uu));
+                    const uint32_t n = v ? 16u : 0u;
+#pragma unroll
+                    for (int ch = 0; ch < kChunks; ++ch)
+                        cp_async_16(dst + ch * kChunkBytes, src + ch * 128, n);
+                    // rows 4 wl + q + 8 j (q = lane / 8) of this warp
+                    const uint32_t b = __ballot_sync(0xffffffffu, v);
+                    const uint64_t bits = (b & 1u) | ((b >> 7) & 2u) | ((b >> 14) & 4u) | ((b >> 21) & 8u);
+                    mask |= bits << (4 * wl + 8 * j);
+                }
+                if (bad) atomicCAS(p.error_word, 0, MLA_ERR_BAD_INDEX);
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                if (lane == 0) key_part[2 * st + wl] = mask;
+                warp_arrive(&bars->kv_full[st]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+                skip2(c);
+            }
+        }
     } else if (warp >= 2) {
         // ------------------------------------- softmax / correction / epilogue
         const int q4 = warp & 3;
@@ -623,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         alive = false;
                         break;
                     }
-                    keys = static_cast<uint32_t>(key_mask[st] >> (32 * half));
+                    keys = static_cast<uint32_t>((key_part[2 * st] | key_part[2 * st + 1]) >>
+                                                 (32 * half));
                 } else {
                     const int n = lim - (blk * kPage + 32 * half);
                     keys = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);

@@ -65,13 +65,15 @@ struct DecodeParams {
     // Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11): the kernel's requests
     // are the (i, s) query tokens, each with its own key list of topk
     // physical positions indices[(i * fold + s) * topk + k] (< 0: padding),
-    // gathered through a 2-D [num_tokens x 576] row map of the cache.
+    // gathered row by row from the cache (pages packed back to back).
     // sparse == 0: dense decode through block_table.  (indices may be null
     // when topk == 0.)
     int sparse;
     const int32_t* indices;
     int topk;
     int64_t num_tokens;  // num_pages * 64: positions past it are reported
+    const uint8_t* kv_bytes;  // cache base; row n starts at kv_bytes + n * kv_token_bytes
+    int64_t kv_token_bytes;
     int fold;            // sparse: s_q of the caller (request r = i * fold + s); dense: 0
 };
 

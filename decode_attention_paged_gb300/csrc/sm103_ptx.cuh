@@ -124,19 +124,6 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* ba
         "l"(policy)
         : "memory");
 }
-// Row gather of a 2-D tensor map whose box is {cols, 1}: rows r0..r3 (any
-// order, out-of-range rows read as zeros) land as four consecutive box rows
-// at dst, with the map's swizzle.
-__device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* bar, void* dst,
-                                            int col, int r0, int r1, int r2, int r3,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::"
-        "bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1),
-        "r"(r2), "r"(r3), "l"(policy)
-        : "memory");
-}
 // Ask L2 to fetch one 3-D tile of a tensor map (no shared memory, no
 // completion tracking); a later TMA load of the same tile then hits L2.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1,
@@ -145,6 +132,16 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c
                      reinterpret_cast<uint64_t>(map)),
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
+}
+// 16-byte global -> shared copy through L2 only; src_bytes = 0 reads nothing
+// and fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads).
