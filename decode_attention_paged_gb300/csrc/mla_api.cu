@@ -363,6 +363,7 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.causal = causal;
     p.error_word = d->error_word;
     p.budget_ns = g_budget_ns.load();
+    p.stage_p = p.n_mtiles == 1 ? 1 : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int kind = g_kernel.load();
@@ -547,6 +548,7 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     p.kv_bytes = static_cast<const uint8_t*>(k_cache_dev);
     p.kv_token_bytes = k_token_stride * 2;
     p.fold = s_q;
+    p.stage_p = p.n_mtiles == 1 ? 1 : 0;
     cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, nreq, R, parts,

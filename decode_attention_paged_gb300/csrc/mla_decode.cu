@@ -31,6 +31,14 @@
 //     and MMA issuer (converged warp, elect.sync), warps 2..5 = softmax /
 //     correction / epilogue (one thread per TMEM lane), warps 6..9 = row
 //     gather for sparse decode (idle in dense decode).
+//   - P of a page goes either into that page's RoPE chunk, dead once its
+//     QK^T is done (the softmax of page g + 1 then waits for PV(g) only when
+//     O must be rescaled), or into one P buffer placed after everything else,
+//     which costs 8 KB more shared memory.  The host picks the first for
+//     single-tile problems: the smaller footprint measured 18% faster on a
+//     long ragged batch (the 8 KB alone made that difference).  With two or
+//     more tiles the P buffer measured 2-5% faster: the PV then does not read
+//     P and V from the same stage.
 //   - Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11) gathers each key row
 //     with 16-byte cp.async copies, eight threads per row: measured on GB300
 //     at the rate of the tiled TMA page load, while row-gather TMA copies
@@ -86,20 +94,24 @@ struct Barriers {
     uint64_t kv_empty[kStages];
     uint64_t q_full, q_empty;
     uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, pv_done, o_free, drain;
+    uint64_t p_full[2], pv_done[2];
+    uint64_t o_free, drain;
 };
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
+// After the KV ring: the one P buffer (only in launches that use it), then
+// the barriers, the pair-exchange slots (uint2 [2][128]) and the misc words
+// (tmem base, abort flag, key masks).  The P buffer sits 8 KB-aligned right
+// after the ring: placed elsewhere the PV MMAs measured a few percent slower.
 constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffP + kPBytes;
-constexpr uint32_t kOffXch = kOffBar + 256;            // uint2 [2][128]: pair exchange
-constexpr uint32_t kOffMisc = kOffXch + 2 * 128 * 8;    // tmem base, abort flag, key masks
-constexpr uint32_t kSmemBytes = kOffMisc + 64;
+constexpr uint32_t kTailBytes = 256 + 2 * 128 * 8 + 64;
+constexpr uint32_t kSmemBytes = kOffP + kTailBytes;             // P in each page's RoPE chunk
+constexpr uint32_t kSmemBytesP = kOffP + kPBytes + kTailBytes;  // with the P buffer
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 static_assert(kChunks % 3 == 0, "QK^T is issued three chunks per turn");
-static_assert(kSmemBytes < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+static_assert(kSmemBytesP < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
+static_assert(kSmemBytesP <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 
 struct Part {
     int begin_req, end_req, begin_block, end_block, begin_split;
@@ -242,6 +254,8 @@ __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t
 
 }  // namespace
 
+// kStageP: P of each page in that page's RoPE chunk (else the one P buffer).
+template <bool kStageP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap kv_map) {
@@ -252,14 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sKV = smem + kOffKV;
     uint8_t* sP = smem + kOffP;
-    Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
-    uint2* xch = reinterpret_cast<uint2*>(smem + kOffXch);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    uint8_t* tail = smem + kOffP + (kStageP ? 0u : kPBytes);
+    Barriers* bars = reinterpret_cast<Barriers*>(tail);
+    uint2* xch = reinterpret_cast<uint2*>(tail + 256);
+    uint8_t* misc = tail + 256 + 2 * 128 * 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     // Sparse decode: key_part[2 * stage + w] has bit t set when stage row t
     // holds a key; the two gather warps of a stage own disjoint bits (written
     // before their kv_full arrivals).
-    volatile uint64_t* key_part = reinterpret_cast<volatile uint64_t*>(smem + kOffMisc + 8);
+    volatile uint64_t* key_part = reinterpret_cast<volatile uint64_t*>(misc + 8);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
@@ -275,8 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_full[s], 1);
             mbar_init(&bars->s_empty[s], 4);
         }
-        mbar_init(&bars->p_full, 4);
-        mbar_init(&bars->pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->p_full[b], 4);
+            mbar_init(&bars->pv_done[b], 1);
+        }
         mbar_init(&bars->o_free, 4);
         mbar_init(&bars->drain, 1);
         fence_barrier_init();
@@ -422,7 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dK1 = smem_desc(smem_u32(sKV + kStageBytes), 16, 1024);
         const uint64_t dV0 = smem_desc(smem_u32(sKV), kChunkBytes, 1024);
         const uint64_t dV1 = smem_desc(smem_u32(sKV + kStageBytes), kChunkBytes, 1024);
-        const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024);
+        // P(g): page g's RoPE chunk (dead once QK^T(g) is done) when
+        // kStageP, else the one P buffer.
+        const uint64_t dP0 = smem_desc(smem_u32(kStageP ? sKV + 8 * kChunkBytes : sP), 16, 1024);
+        const uint64_t dP1 =
+            smem_desc(smem_u32(kStageP ? sKV + kStageBytes + 8 * kChunkBytes : sP), 16, 1024);
         const uint32_t tS0 = tmem + kColS, tS1 = tmem + kColS + 32;
         const uint32_t tO0 = tmem + kColO, tO1 = tmem + kColO + 128;
         constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
@@ -437,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool first = pv.blk == pv.b0;
                 bool ready = false;
                 if (leader) {
-                    ready = mbar_test_wait(&bars->p_full, pv.g & 1);
+                    ready = mbar_test_wait(&bars->p_full[pv.g & 1], (pv.g >> 1) & 1);
                     if (ready && first && pv.item > 0)
                         ready = mbar_test_wait(&bars->o_free, (pv.item - 1) & 1);
                 }
@@ -445,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ready) {
                     tc_fence_after();
                     const uint64_t bV = (pv.g & 1) ? dV1 : dV0;
+                    const uint64_t dP = (pv.g & 1) ? dP1 : dP0;
                     const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -454,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk, idesc_pv, acc);
                     }
                     if (elect_one()) {
-                        mma_commit(&bars->pv_done);
+                        mma_commit(&bars->pv_done[pv.g & 1]);
                         mma_commit(&bars->kv_empty[pv.g & 1]);
                     }
                     __syncwarp();
@@ -683,13 +706,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_part += psum;
 
-                // The P buffer and O are free once the previous PV finished.
-                if (gblk > 0 && !warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
-                    alive = false;
-                    break;
+                // With P in page g's own RoPE chunk (kStageP), only a
+                // rescale of O has to wait for PV(g - 1); otherwise the wait
+                // is for PV(g - 2): PV may trail by at most two pages, which
+                // keeps the parity waits on the two pv_done barriers
+                // unambiguous.  With the one P buffer, P(g) waits for PV(g - 1).
+                const bool rescale = __any_sync(0xffffffffu, need && blk > b0);
+                const uint32_t lag = (kStageP && !rescale) ? 2u : 1u;
+                if (gblk >= lag) {
+                    const uint32_t w = gblk - lag;
+                    if (!warp_wait(&bars->pv_done[w & 1], (w >> 1) & 1, wc)) {
+                        alive = false;
+                        break;
+                    }
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need && blk > b0)) {
+                if (rescale) {
                     const float a = (need && blk > b0) ? alpha : 1.f;
 #pragma unroll 1
                     for (int cg = 0; cg < 8; ++cg) {
@@ -718,12 +750,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t off = sw128_offset(r, 4 * half + k);
-                    *reinterpret_cast<uint4*>(sP + off) =
+                    *reinterpret_cast<uint4*>(
+                        (kStageP ? sKV + st * kStageBytes + 8 * kChunkBytes : sP) + off) =
                         make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                warp_arrive(&bars->p_full);
+                warp_arrive(&bars->p_full[st]);
             }
             if (!alive) break;
 
@@ -731,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool has_blocks = b1 > b0;
             float l_tot = 0.f;
             if (has_blocks) {
-                if (!warp_wait(&bars->pv_done, (gblk - 1) & 1, wc)) {
+                const uint32_t w = gblk - 1;
+                if (!warp_wait(&bars->pv_done[w & 1], (w >> 1) & 1, wc)) {
                     alive = false;
                     break;
                 }
@@ -813,22 +847,26 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(configured_mask & (1 << dev))) {
-        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytesP));
         if (e != cudaSuccess) return e;
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_mtiles, p.num_parts, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = p.stage_p ? kSmemBytes : kSmemBytesP;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel, p, q_map, kv_map);
+    return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, p, q_map, kv_map)
+                     : cudaLaunchKernelEx(&cfg, decode_kernel<false>, p, q_map, kv_map);
 }
 
 }  // namespace mla

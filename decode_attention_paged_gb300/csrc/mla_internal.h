@@ -75,6 +75,9 @@ struct DecodeParams {
     const uint8_t* kv_bytes;  // cache base; row n starts at kv_bytes + n * kv_token_bytes
     int64_t kv_token_bytes;
     int fold;            // sparse: s_q of the caller (request r = i * fold + s); dense: 0
+    // decode_kernel only: 1 = P of each page in that page's RoPE chunk (the
+    // softmax may run a page ahead of PV), 0 = one P buffer.
+    int stage_p;
 };
 
 // Output address of (request r, row) for both layouts: dense rows are
