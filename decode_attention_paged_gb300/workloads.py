@@ -248,3 +248,75 @@ def sparse_hbm_bytes(indices: torch.Tensor, h_q: int) -> int:
     b, s_q, _ = indices.shape
     rows = b * s_q * h_q
     return int((indices >= 0).sum().item()) * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)
+
+
+# ------------------------------------------------------------ FP8 KV cache
+# FP8 cache layout ("[DeepSeek-3] FlashMLA", sec. 12): 656 bytes per token,
+# 512 float8_e4m3 latent values, 4 fp32 scales (one per 128 latent values),
+# then the 64 RoPE values in bf16.  The decode path only reads this layout;
+# writing it is the cache writer's job, done here with torch's own float8
+# conversion so that synthetic FP8 caches can be drawn.
+FP8_ROW_BYTES = 656
+E4M3_MAX = 448.0
+
+
+def fp8_cache(k_cache: torch.Tensor) -> torch.Tensor:
+    """[pages, 64, 1, 576] bf16 -> [pages, 64, 1, 656] uint8: per 128-value tile
+    scale = amax / 448, latent = e4m3(x / scale), RoPE copied."""
+    assert k_cache.dtype == torch.bfloat16 and k_cache.shape[-1] == D_QK
+    lead = k_cache.shape[:-1]
+    x = k_cache[..., :512].float().reshape(*lead, 4, 128)
+    amax = x.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q8 = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    out = torch.empty(*lead, FP8_ROW_BYTES, dtype=torch.uint8)
+    out[..., :512] = q8.reshape(*lead, 512).view(torch.uint8)
+    out[..., 512:528] = scale.reshape(*lead, 4).contiguous().view(torch.uint8)
+    out[..., 528:] = k_cache[..., 512:].contiguous().view(torch.uint8)
+    return out
+
+
+@dataclasses.dataclass
+class Fp8Workload:
+    """A decode workload whose cache is stored in the FP8 layout."""
+    name: str
+    q: torch.Tensor            # [b, s_q, h_q, 576] bf16
+    k_cache: torch.Tensor      # [num_pages, 64, 1, 656] uint8
+    block_table: torch.Tensor  # [b, max_blocks] int32
+    cache_seqlens: torch.Tensor
+    softmax_scale: float
+    causal: bool
+
+    @property
+    def b(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def s_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def h_q(self) -> int:
+        return self.q.shape[2]
+
+    def to(self, device) -> "Fp8Workload":
+        return dataclasses.replace(
+            self, q=self.q.to(device), k_cache=self.k_cache.to(device),
+            block_table=self.block_table.to(device), cache_seqlens=self.cache_seqlens.to(device))
+
+
+def as_fp8(w: Workload) -> Fp8Workload:
+    return Fp8Workload(w.name + " fp8", w.q, fp8_cache(w.k_cache), w.block_table,
+                       w.cache_seqlens, w.softmax_scale, w.causal)
+
+
+def memory_bound_fp8(seed_offset: int = 0) -> Fp8Workload:
+    """The memory-bound workload with its cache in the FP8 layout."""
+    return as_fp8(memory_bound(seed_offset))
+
+
+def fp8_hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int) -> int:
+    """Algorithmic bytes with the FP8 cache: 656 B per cached token read once,
+    plus q in, out and lse out."""
+    rows = len(seqlens) * s_q * h_q
+    return sum(int(L) for L in seqlens) * FP8_ROW_BYTES + rows * (D_QK * 2 + D_V * 2 + 4)

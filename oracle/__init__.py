@@ -4,7 +4,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
 Python binding) never imports, links or calls it, and shares no code with it.
 
-The C sources (``mla_oracle.c``, ``sparse_oracle.c``, ``plan_oracle.c``) hold the arithmetic and
+The C sources (``mla_oracle.c``, ``sparse_oracle.c``, ``plan_oracle.c``, ``fp8_oracle.c``) hold the arithmetic and
 cite the pages they follow; this module only compiles them with gcc and
 marshals numpy arrays through ctypes.
 
@@ -23,7 +23,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
 _SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "sparse_oracle.c"),
-         os.path.join(_HERE, "plan_oracle.c")]
+         os.path.join(_HERE, "plan_oracle.c"), os.path.join(_HERE, "fp8_oracle.c")]
 _lock = threading.Lock()
 _lib = None
 
@@ -71,6 +71,12 @@ def _load():
             lib.oracle_mla_sparse_rows.restype = I
             lib.oracle_plan.argtypes = [P, I, I, I, I, P, P]
             lib.oracle_plan.restype = I
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = D
+            lib.oracle_bf16_round.argtypes = [D]
+            lib.oracle_bf16_round.restype = ctypes.c_uint16
+            lib.oracle_fp8_dequant.argtypes = [P, I64, I64, P]
+            lib.oracle_fp8_dequant.restype = I
             _lib = lib
     return _lib
 
@@ -251,3 +257,38 @@ def mla_sparse_rows(p: SparseProblem, units, dv: int = 512, nthreads: int = 1):
     if st != 0:
         raise RuntimeError(f"oracle_mla_sparse_rows failed: {st}")
     return out, lse
+
+
+# ------------------------------------------------------------ FP8 KV cache
+FP8_ROW_BYTES = 656  # 512 e4m3 + 4 fp32 scales + 64 bf16 ("[DeepSeek-3] FlashMLA", sec. 12)
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one float8_e4m3 code (fp8_oracle.c)."""
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def bf16_round(x: float) -> int:
+    """bf16 bit pattern of x rounded to nearest even (fp8_oracle.c)."""
+    return int(_load().oracle_bf16_round(float(x)))
+
+
+def fp8_dequant(cache_bytes) -> np.ndarray:
+    """FP8 cache [pages, 64, 1, 656] uint8 (numpy or torch) -> bf16 bit patterns
+    [pages, 64, 1, 576] of the dequantised rows."""
+    a = cache_bytes.cpu().numpy() if hasattr(cache_bytes, "cpu") else np.asarray(cache_bytes)
+    a = np.ascontiguousarray(a, dtype=np.uint8)
+    assert a.shape[-1] == FP8_ROW_BYTES
+    n = a.size // FP8_ROW_BYTES
+    out = np.empty(a.shape[:-1] + (576,), dtype=np.uint16)
+    st = _load().oracle_fp8_dequant(_ptr(a), n, FP8_ROW_BYTES, _ptr(out))
+    if st != 0:
+        raise RuntimeError(f"oracle_fp8_dequant failed: {st}")
+    return out
+
+
+def mla_decode_fp8(q_bits, cache_bytes, block_table, cache_seqlens, scale, causal,
+                   dv: int = 512, nthreads: int = 1):
+    """Dense decode over an FP8 cache: the dense oracle on the dequantised rows."""
+    p = Problem(q_bits, fp8_dequant(cache_bytes), block_table, cache_seqlens, scale, causal)
+    return mla_decode(p, dv, nthreads)
