@@ -303,6 +303,25 @@ def measure_sparse(w, torch, api, W_mod, K, Wup):
     return res
 
 
+def measure_fp8(w, torch, api, W_mod, K, Wup):
+    """Decode over the FP8-layout cache: mla_decode_fp8_fwd steps in a CUDA
+    graph; the plan is built once, outside the timed steps."""
+    g = w.to("cuda")
+    meta, ns = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
+    call = api.Fp8DecodeCall(g.q, g.k_cache, g.block_table, g.cache_seqlens, w.softmax_scale,
+                             w.causal, meta, ns)
+    gr = capture(torch, call.fwd)
+    assert api.mla_last_device_error() == 0
+    ms_total, _ = time_steps(torch, gr, K, Wup)
+    code = api.mla_last_device_error()
+    assert code == 0, f"device error {code}"
+    sl = w.cache_seqlens.tolist()
+    res = {"ms_per_step": ms_total / K, "flops": W_mod.flops(sl, w.s_q, w.h_q, w.causal),
+           "bytes": W_mod.fp8_hbm_bytes(sl, w.s_q, w.h_q), "tokens": sum(sl)}
+    del gr, call, g
+    return res
+
+
 def e2e_measure(w, torch, api, steps):
     """Public API from pinned host buffers, copies inside the timed region."""
     host = {
@@ -520,6 +539,18 @@ def main():
             }
             del gx, cx
             torch.cuda.empty_cache()
+        wf = W_mod.memory_bound_fp8()
+        kx = max(50, min(args.steps, 1000))
+        r = measure_fp8(wf, torch, api, W_mod, kx, 5)
+        t_s = r["ms_per_step"] * 1e-3
+        extra["memory_bound_fp8"] = {
+            "workload": wf.name, "ms_per_step": r["ms_per_step"],
+            "step_gbs": r["bytes"] / t_s / 1e9, "step_tflops": r["flops"] / t_s / 1e12,
+            "frac_hbm_peak": r["bytes"] / t_s / 1e9 / hbm_peak,
+            "tokens_per_s": r["tokens"] / t_s, "steps": kx,
+        }
+        del wf
+        torch.cuda.empty_cache()
         ws = W_mod.sparse()
         kx = max(50, min(args.steps, 1000))
         r = measure_sparse(ws, torch, api, W_mod, kx, 5)

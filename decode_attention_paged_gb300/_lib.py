@@ -44,6 +44,8 @@ SIGNATURES = {
     "mla_decode_combine": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _P, _I64, _I64, _I64, _P, _P]),
     "mla_decode_fwd_noalloc": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I,
                                     _I, _I, _F, _I, _P, _P, _P, _I64, _I64, _I64, _P, _P]),
+    "mla_decode_fp8_fwd": (_I, [_P, _I64, _P, _I64, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _F,
+                                _I, _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P, _P]),
     "mla_metadata_size_sparse": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "mla_get_metadata_sparse": (_I, [_I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_workspace_size_sparse": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ)]),

@@ -163,6 +163,58 @@ def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: 
     return out, lse
 
 
+class Fp8DecodeCall:
+    """Marshalled arguments of one decode over an FP8-layout cache
+    (include/mla_decode.h, mla_decode_fp8_fwd): k_cache uint8
+    [pages, 64, 1, 656] with packed rows."""
+
+    def __init__(self, q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                 num_splits, workspace=None, out=None, lse=None, stream=None):
+        assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.uint8
+        assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+        b, s_q, h_q, d = q.shape
+        assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
+            q.stride(1) == h_q * D_QK
+        num_pages, page, h_kv, row = k_cache.shape
+        assert row == 656 and k_cache.stride(3) == 1 and k_cache.stride(1) == 656 * h_kv
+        assert block_table.stride(1) == 1
+        dev = q.device
+        with torch.cuda.device(dev):
+            if out is None:
+                out = torch.empty(b, s_q, h_q, D_V, dtype=torch.bfloat16, device=dev)
+            if lse is None:
+                lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
+            assert out.stride(3) == 1 and lse.is_contiguous()
+            if workspace is None:
+                workspace = torch.empty(workspace_size(b, h_q, s_q, h_kv), dtype=torch.uint8,
+                                        device=dev)
+        cache_seqlens = cache_seqlens.contiguous()
+        self.device = dev
+        self.out, self.lse, self.workspace = out, lse, workspace
+        self._keep = (q, k_cache, block_table, cache_seqlens, meta, num_splits)
+        self.stream = stream
+        self.args = (
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), num_pages, page,
+            _ptr(block_table), block_table.stride(0), block_table.shape[1], _ptr(cache_seqlens), b,
+            s_q, h_q, h_kv, float(softmax_scale), int(bool(causal)), _ptr(meta), _ptr(num_splits),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+            out.stride(0), out.stride(1), out.stride(2), _ptr(lse))
+
+    def fwd(self):
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.load().mla_decode_fp8_fwd(*self.args, _stream_ptr(self.stream)),
+                       "mla_decode_fp8_fwd")
+        return self.out, self.lse
+
+
+def mla_decode_fp8_fwd(q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                       num_splits, workspace=None, out=None, lse=None, stream=None):
+    """Decode over an FP8-layout cache (656-byte rows: e4m3 latent, fp32
+    scales, bf16 RoPE); the metadata is mla_get_metadata's."""
+    return Fp8DecodeCall(q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
+                         num_splits, workspace, out, lse, stream).fwd()
+
+
 def metadata_size_sparse(batch: int, h_q: int, s_q: int, h_kv: int = 1) -> Tuple[int, int]:
     mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     _lib.check(_lib.load().mla_metadata_size_sparse(batch, h_q, s_q, h_kv, ctypes.byref(mb),

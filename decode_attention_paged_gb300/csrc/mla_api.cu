@@ -556,6 +556,89 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
                         lse_dev, stream);
 }
 
+int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                       int64_t k_page_stride_bytes, int num_pages, int page_size,
+                       const int32_t* block_table_dev, int64_t bt_batch_stride,
+                       int max_blocks_per_seq, const int32_t* cache_seqlens_dev, int batch,
+                       int s_q, int h_q, int h_kv, float softmax_scale, int causal,
+                       const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
+                       size_t workspace_bytes, void* out_dev, int64_t out_batch_stride,
+                       int64_t out_s_stride, int64_t out_h_stride, float* lse_dev,
+                       mla_stream_t stream) {
+    constexpr int64_t kRow = 656, kPageBytes = 64 * kRow;
+    int st = check_shape(batch, h_q, s_q, h_kv);
+    if (st) return st;
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    // The FP8 layout is read by the single-CTA kernel, whose plan the pair
+    // kernel's metadata does not match.
+    if (g_kernel.load() == MLA_KERNEL_PAIR) return MLA_ERR_UNSUPPORTED;
+    if (!q_dev || !k_cache_dev || !block_table_dev || !cache_seqlens_dev || !meta_dev ||
+        !num_splits_dev || !out_dev || !lse_dev)
+        return MLA_ERR_INVALID_ARGUMENT;
+    if (num_pages < 1 || static_cast<int64_t>(num_pages) * kPage > INT32_MAX ||
+        max_blocks_per_seq < 1 || bt_batch_stride < max_blocks_per_seq ||
+        q_batch_stride < static_cast<int64_t>(s_q) * h_q * kDqk ||
+        k_page_stride_bytes < kPageBytes || out_h_stride < kDv ||
+        out_s_stride < out_h_stride * h_q || out_batch_stride < out_s_stride * s_q ||
+        !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
+        return MLA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_dev) || !aligned16(k_cache_dev) || !aligned16(out_dev) ||
+        (q_batch_stride % 8) || (k_page_stride_bytes % 16) || (out_batch_stride % 8) ||
+        (out_s_stride % 8) || (out_h_stride % 8) || (reinterpret_cast<uintptr_t>(lse_dev) & 3u))
+        return MLA_ERR_BAD_ALIGNMENT;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const int R = s_q * h_q;
+    const int parts = num_parts_single(R, d);
+    size_t o_bytes = 0, ws_need = 0;
+    workspace_layout(batch, R, parts, &o_bytes, &ws_need);
+    if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+    if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
+
+    CUtensorMap q_map;
+    const uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
+    st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
+                   kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
+    if (st) return st;
+
+    DecodeParams p{};
+    p.block_table = block_table_dev;
+    p.bt_stride = bt_batch_stride;
+    p.max_blocks = max_blocks_per_seq;
+    p.seqlens = cache_seqlens_dev;
+    p.meta = static_cast<const int32_t*>(meta_dev);
+    p.num_splits = num_splits_dev;
+    p.out = static_cast<__nv_bfloat16*>(out_dev);
+    p.out_sb = out_batch_stride;
+    p.out_ss = out_s_stride;
+    p.out_sh = out_h_stride;
+    p.lse = lse_dev;
+    p.oaccum = static_cast<float*>(workspace_dev);
+    p.lseaccum = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + o_bytes);
+    p.batch = batch;
+    p.s_q = s_q;
+    p.h_q = h_q;
+    p.R = R;
+    p.n_mtiles = n_mtiles_of(R);
+    p.num_parts = parts;
+    p.q_box_rows = static_cast<int>(q_box_rows);
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.causal = causal;
+    p.error_word = d->error_word;
+    p.budget_ns = g_budget_ns.load();
+    p.fp8 = 1;
+    p.kv_bytes = static_cast<const uint8_t*>(k_cache_dev);
+    p.kv_page_bytes = k_page_stride_bytes;
+    p.num_tokens = static_cast<int64_t>(num_pages) * kPage;
+    p.stage_p = p.n_mtiles == 1 ? 1 : 0;
+    // (The kernel takes a page tensor map too; the FP8 path never reads it.)
+    cudaError_t e = launch_decode(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R, parts,
+                        s_q, h_q, 0, out_dev, out_batch_stride, out_s_stride, out_h_stride,
+                        lse_dev, stream);
+}
+
 int mla_last_device_error(mla_stream_t stream, int* code) {
     if (!code) return MLA_ERR_INVALID_ARGUMENT;
     DeviceInfo* d = nullptr;

@@ -54,6 +54,8 @@
 //     MLA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
 //     returns.  Waits in the softmax warps are taken by lane 0 and broadcast,
 //     so control flow stays warp-uniform.
+#include <cuda_fp8.h>
+
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -96,8 +98,16 @@ struct Barriers {
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full[2], pv_done[2];
     uint64_t o_free, drain;
+    uint64_t raw_full[kStages];  // FP8: a page's raw rows have landed
 };
 
+// FP8 cache: a page's 64 raw rows of 656 bytes land at the top of its stage
+// and are dequantised in place into the bf16 layout below them.
+constexpr uint32_t kFp8RowBytes = 656;
+constexpr uint32_t kFp8PageBytes = kPage * kFp8RowBytes;  // 41984
+constexpr uint32_t kRawOff = kStageBytes - kFp8PageBytes;  // 31744, 16-byte aligned
+static_assert(kRawOff % 16 == 0 && kFp8PageBytes % 16 == 0, "bulk copy alignment");
+constexpr uint32_t kDequantBar = 1;  // named barrier of the four dequant warps
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 // After the KV ring: the one P buffer (only in launches that use it), then
@@ -255,7 +265,9 @@ __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t
 }  // namespace
 
 // kStageP: P of each page in that page's RoPE chunk (else the one P buffer).
-template <bool kStageP>
+// kFp8: the cache is in the FP8 layout (its own instantiation: the dequant
+// registers would otherwise raise every launch's register count).
+template <bool kStageP, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap kv_map) {
@@ -276,13 +288,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // holds a key; the two gather warps of a stage own disjoint bits (written
     // before their kv_full arrivals).
     volatile uint64_t* key_part = reinterpret_cast<volatile uint64_t*>(misc + 8);
+    // FP8: raw_bad[stage] = 1 when that page lies outside the cache.
+    volatile int* raw_bad = reinterpret_cast<volatile int*>(misc + 40);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->kv_full[s], p.sparse ? 2 : 1);
+            mbar_init(&bars->kv_full[s], kFp8 ? 4 : (p.sparse ? 2 : 1));
+            mbar_init(&bars->raw_full[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
         mbar_init(&bars->q_full, 1);
@@ -384,11 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = ld.g & 1;
                 if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
                     uint8_t* dst = sKV + st * kStageBytes;
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c, 0,
-                                    page, policy);
+                    if (kFp8) {
+                        // One copy of the page's raw rows; a page outside the
+                        // cache is not read and dequantises to zeros (as the
+                        // bf16 path's out-of-range tile reads zeros).
+                        const bool in =
+                            page >= 0 && static_cast<int64_t>(page) * kPage < p.num_tokens;
+                        raw_bad[st] = in ? 0 : 1;
+                        if (in) {
+                            mbar_arrive_expect_tx(&bars->raw_full[st], kFp8PageBytes);
+                            bulk_load(dst + kRawOff,
+                                      p.kv_bytes + static_cast<int64_t>(page) * p.kv_page_bytes,
+                                      kFp8PageBytes, &bars->raw_full[st], policy);
+                        } else {
+                            mbar_arrive(&bars->raw_full[st]);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
+                                        0, page, policy);
+                    }
                 }
                 __syncwarp();
                 ++n_kv;
@@ -415,7 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Drain: never leave the CTA with copies still landing in its smem.
         if (lane == 0) {
             for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)
-                mbar_drain(&bars->kv_full[k & 1], (k >> 1) & 1, kDrainBudgetNs);
+                mbar_drain(kFp8 ? &bars->raw_full[k & 1] : &bars->kv_full[k & 1], (k >> 1) & 1,
+                           kDrainBudgetNs);
             if (n_q > 0) mbar_drain(&bars->q_full, (n_q - 1) & 1, kDrainBudgetNs);
         }
         __syncwarp();
@@ -619,6 +652,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
                 skip2(c);
+            }
+        } else if (kFp8) {
+            // ---------------------------------------- FP8 page dequantisation
+            // Two threads per cached row: thread (t, hh) takes latent dims
+            // [256 hh, 256 hh + 256) with their two scales and RoPE dims
+            // [32 hh, 32 hh + 32).  The raw rows sit in the top of the stage
+            // that the bf16 rows overwrite, so every thread reads all its raw
+            // bytes before any thread writes (a named barrier of these four
+            // warps, whose exits are agreed through bar.red.and).  Each value
+            // becomes bf16(e4m3 * scale): the e4m3 -> f16 conversion is exact,
+            // the product is rounded to fp32, then to bf16 (nearest even).
+            const int dt = tid - 32 * kGatherWarp0;
+            const int t = dt >> 1, hh = dt & 1;
+            for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
+                const int st = c.g & 1;
+                const bool ok = warp_wait(&bars->raw_full[st], (c.g >> 1) & 1, wc);
+                if (!named_bar_and(kDequantBar, 128, ok)) break;
+                uint8_t* stage = sKV + st * kStageBytes;
+                const uint8_t* raw = stage + kRawOff + t * kFp8RowBytes;
+                const bool bad = raw_bad[st] != 0;
+                uint4 lat[16], rope[4];
+                float sc[2];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    lat[u] = *reinterpret_cast<const uint4*>(raw + 256 * hh + 16 * u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    rope[u] = *reinterpret_cast<const uint4*>(raw + 528 + 64 * hh + 16 * u);
+                sc[0] = *reinterpret_cast<const float*>(raw + 512 + 8 * hh);
+                sc[1] = *reinterpret_cast<const float*>(raw + 516 + 8 * hh);
+                named_bar_sync(kDequantBar, 128);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float s = sc[u >> 3];
+                    const uint32_t in[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_fp8x2_storage_t two =
+                            static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1)));
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                        o[j] = bad ? 0u : pack_bf16x2(f.x * s, f.y * s);
+                    }
+                    const int dim0 = 256 * hh + 16 * u;  // 16 dims: two 16-byte units
+                    uint8_t* chunk = stage + (dim0 >> 6) * kChunkBytes;
+                    const uint32_t unit = (dim0 & 63) >> 3;
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit + 1)) =
+                        make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                uint8_t* rchunk = stage + 8 * kChunkBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(rchunk + sw128_offset(t, 4 * hh + u)) =
+                        bad ? make_uint4(0, 0, 0, 0) : rope[u];
+                fence_proxy_async_smem();
+                warp_arrive(&bars->kv_full[st]);
             }
         }
     } else if (warp >= 2) {
@@ -847,12 +939,18 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(configured_mask & (1 << dev))) {
-        e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytesP));
-        if (e != cudaSuccess) return e;
+        const void* k_sp[2] = {reinterpret_cast<const void*>(decode_kernel<true, false>),
+                               reinterpret_cast<const void*>(decode_kernel<true, true>)};
+        const void* k_p[2] = {reinterpret_cast<const void*>(decode_kernel<false, false>),
+                              reinterpret_cast<const void*>(decode_kernel<false, true>)};
+        for (int i = 0; i < 2; ++i) {
+            e = cudaFuncSetAttribute(k_sp[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytes));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(k_p[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kSmemBytesP));
+            if (e != cudaSuccess) return e;
+        }
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
     }
     cudaLaunchConfig_t cfg = {};
@@ -865,8 +963,11 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, p, q_map, kv_map)
-                     : cudaLaunchKernelEx(&cfg, decode_kernel<false>, p, q_map, kv_map);
+    if (p.fp8)
+        return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true, true>, p, q_map, kv_map)
+                         : cudaLaunchKernelEx(&cfg, decode_kernel<false, true>, p, q_map, kv_map);
+    return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true, false>, p, q_map, kv_map)
+                     : cudaLaunchKernelEx(&cfg, decode_kernel<false, false>, p, q_map, kv_map);
 }
 
 }  // namespace mla

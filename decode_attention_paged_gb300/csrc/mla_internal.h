@@ -75,6 +75,11 @@ struct DecodeParams {
     const uint8_t* kv_bytes;  // cache base; row n starts at kv_bytes + n * kv_token_bytes
     int64_t kv_token_bytes;
     int fold;            // sparse: s_q of the caller (request r = i * fold + s); dense: 0
+    // FP8 cache ("[DeepSeek-3] FlashMLA", sec. 12; decode_kernel only): rows
+    // of 656 bytes (512 e4m3, 4 fp32 scales, 64 bf16 RoPE), a page of 64 rows
+    // packed at kv_bytes + page * kv_page_bytes; num_tokens = num_pages * 64.
+    int fp8;
+    int64_t kv_page_bytes;
     // decode_kernel only: 1 = P of each page in that page's RoPE chunk (the
     // softmax may run a page ahead of PV), 0 = one P buffer.
     int stage_p;

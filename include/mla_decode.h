@@ -240,6 +240,36 @@ MLA_API int mla_decode_fwd_noalloc(const void *q_dev, int64_t q_batch_stride,
                                    int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
 
 /*
+ * mla_decode_fp8_fwd -- mla_decode_fwd over a cache in the FP8 layout of
+ * "[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐", sec. 12: every
+ * token takes 656 bytes,
+ *     bytes [0, 512)    512 float8_e4m3 values: latent dims 0..511
+ *     bytes [512, 528)  4 fp32 scales, scale j for latent dims 128j..128j+127
+ *     bytes [528, 656)  64 bf16 values: RoPE dims 512..575
+ * The kernel dequantises each row to k[c] = bf16(e4m3 * scale) (c < 512,
+ * round to nearest even) next to the bf16 RoPE and computes what
+ * mla_decode_fwd computes over those rows.
+ *   k_cache_dev  uint8 [num_pages][64][h_kv = 1][656]: the rows of a page
+ *                packed (row stride 656 bytes), pages k_page_stride_bytes
+ *                apart (>= 41984, a multiple of 16); 16-byte aligned.  A
+ *                block-table entry outside [0, num_pages) reads zeros.
+ *   everything else as mla_decode_fwd; the metadata from mla_get_metadata.
+ * Always runs the single-CTA kernel: returns MLA_ERR_UNSUPPORTED while
+ * mla_set_decode_kernel selects MLA_KERNEL_PAIR (whose plan differs).
+ * Enqueues the decode kernel and the combine kernel on `stream`;
+ * graph-capturable.
+ */
+MLA_API int mla_decode_fp8_fwd(const void *q_dev, int64_t q_batch_stride, const void *k_cache_dev,
+                               int64_t k_page_stride_bytes, int num_pages, int page_size,
+                               const int32_t *block_table_dev, int64_t bt_batch_stride,
+                               int max_blocks_per_seq, const int32_t *cache_seqlens_dev,
+                               int batch, int s_q, int h_q, int h_kv, float softmax_scale,
+                               int causal, const void *meta_dev, const int32_t *num_splits_dev,
+                               void *workspace_dev, size_t workspace_bytes, void *out_dev,
+                               int64_t out_batch_stride, int64_t out_s_stride,
+                               int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
+
+/*
  * Sparse decode -- attention over a per-query-token list of selected cache
  * positions instead of a request's whole prefix.  Source: "[DeepSeek-3]
  * FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐", sec. 11 (Sparse FlashMLA: an
