@@ -292,3 +292,30 @@ def mla_decode_fp8(q_bits, cache_bytes, block_table, cache_seqlens, scale, causa
     """Dense decode over an FP8 cache: the dense oracle on the dequantised rows."""
     p = Problem(q_bits, fp8_dequant(cache_bytes), block_table, cache_seqlens, scale, causal)
     return mla_decode(p, dv, nthreads)
+
+
+# ------------------------------------------------------------ h_kv > 1
+def mla_decode_gqa(q_bits, kv_bits, block_table, cache_seqlens, scale, causal, dv: int = 512,
+                   nthreads: int = 1):
+    """Decode with h_kv cache heads ("[DeepSeek-3] FlashMLA", sec. 4: k_cache is
+    [blocks, 64, h_kv, 576]; the dense tests cover MQA and GQA).  Reading: the
+    h_q query heads form h_kv groups of g = h_q / h_kv consecutive heads, and
+    group j attends to cache head j only -- so each group is one dense decode
+    (mla_oracle.c) over that head's rows.
+    q_bits [b, s_q, h_q, 576], kv_bits [pages, 64, h_kv, 576] (bf16 bits).
+    Returns out [b, s_q, h_q, dv], lse [b, h_q, s_q] in fp64."""
+    q_bits = np.asarray(q_bits, dtype=np.uint16)
+    kv_bits = np.asarray(kv_bits, dtype=np.uint16)
+    b, s_q, h_q, d = q_bits.shape
+    h_kv = kv_bits.shape[2]
+    assert h_q % h_kv == 0
+    g = h_q // h_kv
+    out = np.zeros((b, s_q, h_q, dv), dtype=np.float64)
+    lse = np.zeros((b, h_q, s_q), dtype=np.float64)
+    for j in range(h_kv):
+        p = Problem(q_bits[:, :, j * g:(j + 1) * g, :], kv_bits[:, :, j, :], block_table,
+                    cache_seqlens, scale, causal)
+        o, l = mla_decode(p, dv, nthreads)
+        out[:, :, j * g:(j + 1) * g] = o
+        lse[:, j * g:(j + 1) * g] = l
+    return out, lse
