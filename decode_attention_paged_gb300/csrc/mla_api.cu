@@ -90,11 +90,28 @@ int num_parts_single(int R, const DeviceInfo* d) {
     return parts > 0 ? parts : 1;
 }
 
+// Kernel geometry of a dense call: its requests are the (request i, cache
+// head j) pairs, each with the s_q * grp rows of query heads j*grp..j*grp+grp-1.
+struct Geo {
+    int nreq, R, kvh, grp;
+};
+Geo geo_of(int batch, int h_q, int s_q, int h_kv) {
+    return Geo{batch * h_kv, s_q * (h_q / h_kv), h_kv, h_q / h_kv};
+}
+
 int check_shape(int batch, int h_q, int s_q, int h_kv) {
-    if (batch < 1 || h_q < 1 || s_q < 1) return MLA_ERR_INVALID_ARGUMENT;
-    if (batch > sched_max_batch()) return MLA_ERR_UNSUPPORTED;
+    if (batch < 1 || h_q < 1 || s_q < 1 || h_kv < 1) return MLA_ERR_INVALID_ARGUMENT;
+    if (h_q % h_kv != 0) return MLA_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(batch) * h_kv > sched_max_batch()) return MLA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(s_q) * h_q > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
-    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    if (h_kv > 1) {
+        // A query tile covers whole head groups of 64 / grp tokens, or a
+        // 64-head slice of one token; only the single-CTA kernel reads several
+        // cache heads.
+        const int g = h_q / h_kv;
+        if (g <= kTileM ? (kTileM % g != 0) : (g % kTileM != 0)) return MLA_ERR_UNSUPPORTED;
+        if (g_kernel.load() == MLA_KERNEL_PAIR) return MLA_ERR_UNSUPPORTED;
+    }
     return MLA_OK;
 }
 
@@ -130,6 +147,26 @@ bool load_encode() {
             g_encode_status = cudaErrorNotSupported;
     });
     return g_encode_status == cudaSuccess && g_encode != nullptr;
+}
+
+// bf16 tensor map of any rank (2..5): dims[0] contiguous, strides_bytes[k]
+// for dims[k + 1], 128-byte swizzle, zeros out of bounds.
+int encode_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box) {
+    if (!load_encode()) return MLA_ERR_CUDA;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int k = 0; k < rank; ++k) {
+        d[k] = dims[k];
+        b[k] = box[k];
+        e[k] = 1;
+        if (k + 1 < rank) st[k] = strides_bytes[k];
+    }
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                          const_cast<void*>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_INVALID_ARGUMENT;
 }
 
 int encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -198,9 +235,10 @@ int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
     if (st) return st;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int parts = num_parts_of(s_q * h_q, d);
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
+    const int parts = num_parts_of(g.R, d);
     if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
-    if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(batch) + 1);
+    if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(g.nreq) + 1);
     return MLA_OK;
 }
 
@@ -214,11 +252,12 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int R = s_q * h_q;
-    const int parts = num_parts_of(R, d);
-    cudaError_t e = launch_sched(cache_seqlens_dev, -1, batch, R, parts, n_mtiles_of(R),
-                                 g_fixed_overhead.load(), static_cast<int32_t*>(meta_dev),
-                                 num_splits_dev, reinterpret_cast<cudaStream_t>(stream));
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
+    const int parts = num_parts_of(g.R, d);
+    cudaError_t e = launch_sched(cache_seqlens_dev, h_kv, -1, g.nreq, g.R, parts,
+                                 n_mtiles_of(g.R), g_fixed_overhead.load(),
+                                 static_cast<int32_t*>(meta_dev), num_splits_dev,
+                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -228,9 +267,9 @@ int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
     if (!bytes) return MLA_ERR_INVALID_ARGUMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int R = s_q * h_q;
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
     size_t ob = 0;
-    workspace_layout(batch, R, num_parts_of(R, d), &ob, bytes);
+    workspace_layout(g.nreq, g.R, num_parts_of(g.R, d), &ob, bytes);
     return MLA_OK;
 }
 
@@ -240,7 +279,7 @@ namespace {
 
 int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
-                 void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                 int kvh, int grp, void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
                  int64_t out_h_stride, float* lse_dev, mla_stream_t stream);
 
 int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
@@ -258,17 +297,17 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int R = s_q * h_q;
-    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R,
-                        num_parts_of(R, d), s_q, h_q, 0, out_dev, out_batch_stride, out_s_stride,
-                        out_h_stride, lse_dev, stream);
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
+    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, g.nreq, g.R,
+                        num_parts_of(g.R, d), s_q, h_q, 0, g.kvh, g.grp, out_dev,
+                        out_batch_stride, out_s_stride, out_h_stride, lse_dev, stream);
 }
 
 // The combine launch for a plan of `batch` kernel requests of R rows each;
 // fold > 0 for sparse decode (see DecodeParams::fold).
 int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
-                 void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
+                 int kvh, int grp, void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
                  int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(batch, R, parts, &o_bytes, &ws_need);
@@ -289,6 +328,8 @@ int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* work
     c.h_q = h_q;
     c.R = R;
     c.fold = fold;
+    c.kvh = kvh;
+    c.grp = grp;
     cudaError_t e = launch_combine(c, reinterpret_cast<cudaStream_t>(stream), /*pdl=*/true);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -308,7 +349,8 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
         !num_splits_dev || !out_dev || !lse_dev)
         return MLA_ERR_INVALID_ARGUMENT;
     if (num_pages < 1 || max_blocks_per_seq < 1 || bt_batch_stride < max_blocks_per_seq ||
-        q_batch_stride < static_cast<int64_t>(s_q) * h_q * kDqk || k_token_stride < kDqk ||
+        q_batch_stride < static_cast<int64_t>(s_q) * h_q * kDqk ||
+        k_token_stride < static_cast<int64_t>(h_kv) * kDqk ||
         k_page_stride < k_token_stride * kPage || out_h_stride < kDv ||
         out_s_stride < out_h_stride * h_q || out_batch_stride < out_s_stride * s_q ||
         !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
@@ -321,22 +363,49 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int R = s_q * h_q;
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
+    const int R = g.R;
     const int parts = num_parts_of(R, d);
     size_t o_bytes = 0, ws_need = 0;
-    workspace_layout(batch, R, parts, &o_bytes, &ws_need);
+    workspace_layout(g.nreq, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
 
     CUtensorMap q_map, kv_map;
-    const uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
-    st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
-                   kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
-    if (st) return st;
-    st = encode_3d(&kv_map, k_cache_dev, kDqk, kPage, static_cast<uint64_t>(num_pages),
-                   static_cast<uint64_t>(k_token_stride) * 2,
-                   static_cast<uint64_t>(k_page_stride) * 2, kPage);
-    if (st) return st;
+    uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
+    if (h_kv == 1) {
+        st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
+                       kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
+        if (st) return st;
+        st = encode_3d(&kv_map, k_cache_dev, kDqk, kPage, static_cast<uint64_t>(num_pages),
+                       static_cast<uint64_t>(k_token_stride) * 2,
+                       static_cast<uint64_t>(k_page_stride) * 2, kPage);
+        if (st) return st;
+    } else {
+        // Q as (576, grp, h_kv, s_q, b): a box brings a tile's rows s * grp + hh
+        // of one head group (64 / grp tokens, or a 64-head slice of a token).
+        const uint32_t gb = g.grp <= kTileM ? static_cast<uint32_t>(g.grp) : kTileM;
+        const uint32_t sb = g.grp <= kTileM ? static_cast<uint32_t>(
+                                                  s_q < kTileM / g.grp ? s_q : kTileM / g.grp)
+                                            : 1u;
+        q_box_rows = gb * sb;
+        const uint64_t qd[5] = {kDqk, static_cast<uint64_t>(g.grp), static_cast<uint64_t>(h_kv),
+                                static_cast<uint64_t>(s_q), static_cast<uint64_t>(batch)};
+        const uint64_t qs[4] = {kDqk * 2, static_cast<uint64_t>(g.grp) * kDqk * 2,
+                                static_cast<uint64_t>(h_q) * kDqk * 2,
+                                static_cast<uint64_t>(q_batch_stride) * 2};
+        const uint32_t qb[5] = {64, gb, 1, sb, 1};
+        st = encode_bf16(&q_map, q_dev, 5, qd, qs, qb);
+        if (st) return st;
+        // Cache as (576, h_kv, 64, pages): the heads of a token adjacent.
+        const uint64_t kd[4] = {kDqk, static_cast<uint64_t>(h_kv), kPage,
+                                static_cast<uint64_t>(num_pages)};
+        const uint64_t ks[3] = {kDqk * 2, static_cast<uint64_t>(k_token_stride) * 2,
+                                static_cast<uint64_t>(k_page_stride) * 2};
+        const uint32_t kb[4] = {64, 1, kPage, 1};
+        st = encode_bf16(&kv_map, k_cache_dev, 4, kd, ks, kb);
+        if (st) return st;
+    }
 
     DecodeParams p{};
     p.block_table = block_table_dev;
@@ -352,7 +421,7 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.lse = lse_dev;
     p.oaccum = static_cast<float*>(workspace_dev);
     p.lseaccum = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + o_bytes);
-    p.batch = batch;
+    p.batch = g.nreq;
     p.s_q = s_q;
     p.h_q = h_q;
     p.R = R;
@@ -364,11 +433,14 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.error_word = d->error_word;
     p.budget_ns = g_budget_ns.load();
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
+    p.kvh = g.kvh;
+    p.grp = g.grp;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int kind = g_kernel.load();
     if (kind == MLA_KERNEL_AUTO)  // Q mostly in TMEM wins for tiles of at most 32 rows
         kind = R <= 32 ? MLA_KERNEL_TQ : MLA_KERNEL_SINGLE;
+    if (h_kv > 1) kind = MLA_KERNEL_SINGLE;  // the only kernel that reads several cache heads
     cudaError_t e = kind == MLA_KERNEL_PAIR   ? launch_decode_pair(p, q_map, kv_map, s)
                     : kind == MLA_KERNEL_TQ   ? launch_decode_tq(p, q_map, kv_map, s)
                                               : launch_decode(p, q_map, kv_map, s);
@@ -448,7 +520,7 @@ int mla_get_metadata_sparse(int topk, int batch, int h_q, int s_q, int h_kv, voi
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    cudaError_t e = launch_sched(nullptr, topk, batch * s_q, h_q, num_parts_single(h_q, d),
+    cudaError_t e = launch_sched(nullptr, 1, topk, batch * s_q, h_q, num_parts_single(h_q, d),
                                  n_mtiles_of(h_q), g_fixed_overhead.load(),
                                  static_cast<int32_t*>(meta_dev), num_splits_dev,
                                  reinterpret_cast<cudaStream_t>(stream));
@@ -549,11 +621,13 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     p.kv_token_bytes = k_token_stride * 2;
     p.fold = s_q;
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
+    p.kvh = 1;
+    p.grp = h_q;
     cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, nreq, R, parts,
-                        s_q, h_q, s_q, out_dev, out_batch_stride, out_s_stride, out_h_stride,
-                        lse_dev, stream);
+                        s_q, h_q, s_q, 1, h_q, out_dev, out_batch_stride, out_s_stride,
+                        out_h_stride, lse_dev, stream);
 }
 
 int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
@@ -568,6 +642,7 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     constexpr int64_t kRow = 656, kPageBytes = 64 * kRow;
     int st = check_shape(batch, h_q, s_q, h_kv);
     if (st) return st;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
     if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
     // The FP8 layout is read by the single-CTA kernel, whose plan the pair
     // kernel's metadata does not match.
@@ -632,11 +707,13 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     p.num_tokens = static_cast<int64_t>(num_pages) * kPage;
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
     // (The kernel takes a page tensor map too; the FP8 path never reads it.)
+    p.kvh = 1;
+    p.grp = h_q;
     cudaError_t e = launch_decode(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R, parts,
-                        s_q, h_q, 0, out_dev, out_batch_stride, out_s_stride, out_h_stride,
-                        lse_dev, stream);
+                        s_q, h_q, 0, 1, h_q, out_dev, out_batch_stride, out_s_stride,
+                        out_h_stride, lse_dev, stream);
 }
 
 int mla_last_device_error(mla_stream_t stream, int* code) {

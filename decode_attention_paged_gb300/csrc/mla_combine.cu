@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
-    const OutMap om = out_map(req, row, p.h_q, p.s_q, p.fold, p.out_sb, p.out_ss, p.out_sh);
+    const OutMap om =
+        out_map(req, row, p.h_q, p.s_q, p.fold, p.kvh, p.grp, p.out_sb, p.out_ss, p.out_sh);
     __nv_bfloat16* orow = p.out + om.out_off + lane * 16;
     float* lse_out = p.lse + om.lse_idx;
     if (mx == -INFINITY) {

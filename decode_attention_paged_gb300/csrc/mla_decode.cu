@@ -132,9 +132,10 @@ __device__ __forceinline__ int blocks_of(int L) { return L > 0 ? (L + kPage - 1)
 // Blocks [b0, b1) of request `req` that this part owns, clamped to the
 // sequence.  Every role calls this with the same inputs, so all roles see the
 // same list of work items.
+template <bool kHeads>
 __device__ __forceinline__ void item_range(const DecodeParams& p, const Part& part, int req,
                                            int& L, int& nb, int& b0, int& b1) {
-    L = p.sparse ? p.topk : p.seqlens[req];
+    L = p.sparse ? p.topk : p.seqlens[kHeads ? req / p.kvh : req];
     if (L < 0) L = 0;
     nb = blocks_of(L);
     if (nb > p.max_blocks) nb = p.max_blocks;  // reported as MLA_ERR_SEQ_TOO_LONG
@@ -154,10 +155,11 @@ struct Cursor {
     uint32_t item;  // index of the current request among those with blocks
     bool valid;
 };
+template <bool kHeads>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& part, Cursor& c,
                                             int req) {
     for (; req <= part.end_req; ++req) {
-        item_range(p, part, req, c.L, c.nb, c.b0, c.b1);
+        item_range<kHeads>(p, part, req, c.L, c.nb, c.b0, c.b1);
         if (c.b1 > c.b0) {
             c.req = req;
             c.blk = c.b0;
@@ -167,18 +169,20 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& p
     }
     c.valid = false;
 }
+template <bool kHeads>
 __device__ __forceinline__ Cursor cursor_begin(const DecodeParams& p, const Part& part) {
     Cursor c;
     c.g = 0;
     c.item = 0;
-    cursor_seek(p, part, c, part.begin_req);
+    cursor_seek<kHeads>(p, part, c, part.begin_req);
     return c;
 }
+template <bool kHeads>
 __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& part, Cursor& c) {
     ++c.g;
     if (++c.blk < c.b1) return;
     ++c.item;
-    cursor_seek(p, part, c, c.req + 1);
+    cursor_seek<kHeads>(p, part, c, c.req + 1);
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
@@ -267,13 +271,17 @@ __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t
 // kStageP: P of each page in that page's RoPE chunk (else the one P buffer).
 // kFp8: the cache is in the FP8 layout (its own instantiation: the dequant
 // registers would otherwise raise every launch's register count).
-template <bool kStageP, bool kFp8>
+// kHeads: several cache heads (p.kvh > 1); with one head the request and
+// head arithmetic folds away (measured 5% on the h_q = 128 workloads).
+template <bool kStageP, bool kFp8, bool kHeads>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap kv_map) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int mtile = blockIdx.x, part_idx = blockIdx.y;
+    const int kvh = kHeads ? p.kvh : 1;     // cache heads
+    const int grp = kHeads ? p.grp : p.h_q;  // query heads per cache head
 
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sKV = smem + kOffKV;
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0 && !p.sparse) {
         for (int req = part.begin_req; req <= part.end_req; ++req) {
-            const int L = p.seqlens[req];
+            const int L = p.seqlens[req / kvh];
             if (L > 0 && blocks_of(L) > p.max_blocks) raise_error(wc, MLA_ERR_SEQ_TOO_LONG);
         }
     }
@@ -383,13 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
         const bool sparse = p.sparse != 0;
-        Cursor ld = cursor_begin(p, part), ahead = ld;
+        Cursor ld = cursor_begin<kHeads>(p, part), ahead = ld;
         int bid = 0;
         if (!sparse) {
             for (int i = 0; i < 32 && ahead.valid; ++i) {
                 if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-                cursor_next(p, part, ahead);
+                    bid = p.block_table[static_cast<int64_t>(ahead.req / kvh) * p.bt_stride +
+                                        ahead.blk];
+                cursor_next<kHeads>(p, part, ahead);
             }
         }
         uint32_t n_kv = 0, n_q = 0;
@@ -417,9 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
-                                        0, page, policy);
+                        if (!kHeads) {
+                            for (int c = 0; c < kChunks; ++c)
+                                tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes,
+                                            64 * c, 0, page, policy);
+                        } else {  // map (576, h_kv, 64, pages): this request's cache head
+                            for (int c = 0; c < kChunks; ++c)
+                                tma_load_4d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes,
+                                            64 * c, ld.req % kvh, 0, page, policy);
+                        }
                     }
                 }
                 __syncwarp();
@@ -429,9 +444,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ld.item > 0 && !warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
-                                    mtile * kTileM, ld.req, policy);
+                    if (!kHeads) {
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
+                                        mtile * kTileM, ld.req, policy);
+                    } else {
+                        // map (576, grp, h_kv, s_q, b): the tile's rows s * grp + hh
+                        // of head group j; a tile spans 64 / grp tokens, or one
+                        // token's 64-head slice when grp > 64.
+                        const int per_s = grp > kTileM ? grp / kTileM : 1;
+                        const int hh0 = grp > kTileM ? (mtile % per_s) * kTileM : 0;
+                        const int s0 = grp > kTileM ? mtile / per_s : mtile * (kTileM / grp);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_5d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c, hh0,
+                                        ld.req % kvh, s0, ld.req / kvh, policy);
+                    }
                 }
                 __syncwarp();
                 ++n_q;
@@ -439,10 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
             if (!sparse && ahead.valid) {
                 if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-                cursor_next(p, part, ahead);
+                    bid = p.block_table[static_cast<int64_t>(ahead.req / kvh) * p.bt_stride +
+                                        ahead.blk];
+                cursor_next<kHeads>(p, part, ahead);
             }
-            cursor_next(p, part, ld);
+            cursor_next<kHeads>(p, part, ld);
         }
         // Drain: never leave the CTA with copies still landing in its smem.
         if (lane == 0) {
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS0 = tmem + kColS, tS1 = tmem + kColS + 32;
         const uint32_t tO0 = tmem + kColO, tO1 = tmem + kColO + 128;
         constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
-        Cursor qk = cursor_begin(p, part), pv = qk;
+        Cursor qk = cursor_begin<kHeads>(p, part), pv = qk;
         int qk_chunk = 0;  // next 64-dim chunk of QK^T(qk.g) to issue; 0 = not started
         uint64_t idle_since = 0;
         uint32_t idle_spins = 0;
@@ -514,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(&bars->kv_empty[pv.g & 1]);
                     }
                     __syncwarp();
-                    cursor_next(p, part, pv);
+                    cursor_next<kHeads>(p, part, pv);
                     did = true;
                 }
             }
@@ -548,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
                         }
                         __syncwarp();
-                        cursor_next(p, part, qk);
+                        cursor_next<kHeads>(p, part, qk);
                     }
                     did = true;
                 }
@@ -612,11 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             auto skip2 = [&](Cursor& c) {
-                if (c.valid) cursor_next(p, part, c);
-                if (c.valid) cursor_next(p, part, c);
+                if (c.valid) cursor_next<kHeads>(p, part, c);
+                if (c.valid) cursor_next<kHeads>(p, part, c);
             };
-            Cursor c = cursor_begin(p, part);
-            if (grp == 1 && c.valid) cursor_next(p, part, c);
+            Cursor c = cursor_begin<kHeads>(p, part);
+            if (grp == 1 && c.valid) cursor_next<kHeads>(p, part, c);
             load_rows(cur, c);
             while (c.valid) {
                 const int st = c.g & 1;  // == grp
@@ -665,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the product is rounded to fp32, then to bf16 (nearest even).
             const int dt = tid - 32 * kGatherWarp0;
             const int t = dt >> 1, hh = dt & 1;
-            for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
+            for (Cursor c = cursor_begin<kHeads>(p, part); c.valid; cursor_next<kHeads>(p, part, c)) {
                 const int st = c.g & 1;
                 const bool ok = warp_wait(&bars->raw_full[st], (c.g >> 1) & 1, wc);
                 if (!named_bar_and(kDequantBar, 128, ok)) break;
@@ -720,13 +748,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = Lrow & 63, half = Lrow >> 6;
         const int row = mtile * kTileM + r;
         const bool row_valid = row < p.R;
-        const int s_idx = row / p.h_q;  // query token (dense; causal limit)
+        const int s_idx = row / grp;  // query token (dense; causal limit)
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         uint32_t gblk = 0, n_items = 0, xseq = 0;
         bool alive = true;
         for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
             int L, nb, b0, b1;
-            item_range(p, part, req, L, nb, b0, b1);
+            item_range<kHeads>(p, part, req, L, nb, b0, b1);
             int lim = L;
             if (p.causal) {
                 lim = L - p.s_q + s_idx + 1;
@@ -873,7 +901,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = empty ? 0.f : 1.f / l_tot;
             const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
             const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
-            const OutMap om = out_map(req, row, p.h_q, p.s_q, p.fold, p.out_sb, p.out_ss, p.out_sh);
+            const OutMap om = out_map(req, row, p.h_q, p.s_q, p.fold, kvh, grp, p.out_sb,
+                                      p.out_ss, p.out_sh);
             if (has_blocks) {
 #pragma unroll 1
                 for (int cg = 0; cg < 8; ++cg) {
@@ -934,23 +963,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream) {
+    // The instantiations a launch can pick: P placement x {bf16, FP8, bf16
+    // with several cache heads} (FP8 has one cache head).
+    using Kernel = void (*)(DecodeParams, CUtensorMap, CUtensorMap);
+    static const Kernel kernels[2][3] = {
+        {decode_kernel<false, false, false>, decode_kernel<false, true, false>,
+         decode_kernel<false, false, true>},
+        {decode_kernel<true, false, false>, decode_kernel<true, true, false>,
+         decode_kernel<true, false, true>}};
     static int configured_mask = 0;  // per-device "smem attribute set" bits (first 31 devices)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(configured_mask & (1 << dev))) {
-        const void* k_sp[2] = {reinterpret_cast<const void*>(decode_kernel<true, false>),
-                               reinterpret_cast<const void*>(decode_kernel<true, true>)};
-        const void* k_p[2] = {reinterpret_cast<const void*>(decode_kernel<false, false>),
-                              reinterpret_cast<const void*>(decode_kernel<false, true>)};
-        for (int i = 0; i < 2; ++i) {
-            e = cudaFuncSetAttribute(k_sp[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kSmemBytes));
-            if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(k_p[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kSmemBytesP));
-            if (e != cudaSuccess) return e;
-        }
+        for (int sp = 0; sp < 2; ++sp)
+            for (int m = 0; m < 3; ++m) {
+                e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernels[sp][m]),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sp ? kSmemBytes : kSmemBytesP));
+                if (e != cudaSuccess) return e;
+            }
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
     }
     cudaLaunchConfig_t cfg = {};
@@ -963,11 +995,8 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.fp8)
-        return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true, true>, p, q_map, kv_map)
-                         : cudaLaunchKernelEx(&cfg, decode_kernel<false, true>, p, q_map, kv_map);
-    return p.stage_p ? cudaLaunchKernelEx(&cfg, decode_kernel<true, false>, p, q_map, kv_map)
-                     : cudaLaunchKernelEx(&cfg, decode_kernel<false, false>, p, q_map, kv_map);
+    const int mode = p.fp8 ? 1 : (p.kvh > 1 ? 2 : 0);
+    return cudaLaunchKernelEx(&cfg, kernels[p.stage_p ? 1 : 0][mode], p, q_map, kv_map);
 }
 
 }  // namespace mla

@@ -80,28 +80,36 @@ struct DecodeParams {
     // packed at kv_bytes + page * kv_page_bytes; num_tokens = num_pages * 64.
     int fp8;
     int64_t kv_page_bytes;
+    // Cache heads ("[DeepSeek-3] FlashMLA", sec. 4: k_cache [blocks, 64, h_kv,
+    // 576]): dense requests are (i, cache head j) pairs r = i * kvh + j whose
+    // rows are s * grp + hh for query head j * grp + hh (grp = h_q / kvh).
+    // kvh = 1, grp = h_q: one cache head.
+    int kvh, grp;
     // decode_kernel only: 1 = P of each page in that page's RoPE chunk (the
     // softmax may run a page ahead of PV), 0 = one P buffer.
     int stage_p;
 };
 
-// Output address of (request r, row) for both layouts: dense rows are
-// s * h_q + h of request r; sparse requests fold (i, s) and rows are heads.
+// Output address of (kernel request r, row) for every layout: dense
+// requests are (i, cache head j) pairs with rows s * grp + hh (query head
+// j * grp + hh); sparse requests fold (i, s) and their rows are heads.
 struct OutMap {
     int64_t out_off;   // element offset into out
     int64_t lse_idx;   // element index into lse [b][h_q][s_q]
 };
-__device__ __forceinline__ OutMap out_map(int r, int row, int h_q, int s_q, int fold,
-                                          int64_t out_sb, int64_t out_ss, int64_t out_sh) {
+__device__ __forceinline__ OutMap out_map(int r, int row, int h_q, int s_q, int fold, int kvh,
+                                          int grp, int64_t out_sb, int64_t out_ss,
+                                          int64_t out_sh) {
     OutMap m;
     if (fold > 0) {
         const int i = r / fold, s = r % fold;
         m.out_off = i * out_sb + s * out_ss + row * out_sh;
         m.lse_idx = (static_cast<int64_t>(i) * h_q + row) * fold + s;
     } else {
-        const int s = row / h_q, h = row % h_q;
-        m.out_off = r * out_sb + s * out_ss + h * out_sh;
-        m.lse_idx = (static_cast<int64_t>(r) * h_q + h) * s_q + s;
+        const int i = r / kvh, j = r % kvh;
+        const int s = row / grp, h = j * grp + row % grp;
+        m.out_off = i * out_sb + s * out_ss + h * out_sh;
+        m.lse_idx = (static_cast<int64_t>(i) * h_q + h) * s_q + s;
     }
     return m;
 }
@@ -115,14 +123,16 @@ struct CombineParams {
     int64_t out_sb, out_ss, out_sh;
     float* lse;
     int batch, s_q, h_q, R;
-    int fold;  // as DecodeParams::fold
+    int fold;      // as DecodeParams::fold
+    int kvh, grp;  // as DecodeParams::kvh, grp
 };
 
 // Host launchers (return a cudaError_t).
-// seqlens == nullptr: every request has uniform_len keys.
-cudaError_t launch_sched(const int32_t* seqlens, int uniform_len, int batch, int R, int num_parts,
-                         int n_mtiles, int fixed_overhead, int32_t* meta, int32_t* num_splits,
-                         cudaStream_t stream);
+// Request r has seqlens[r / seq_div] keys (seq_div = h_kv: the cache heads
+// of one sequence); seqlens == nullptr: every request has uniform_len keys.
+cudaError_t launch_sched(const int32_t* seqlens, int seq_div, int uniform_len, int batch, int R,
+                         int num_parts, int n_mtiles, int fixed_overhead, int32_t* meta,
+                         int32_t* num_splits, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);
 cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,

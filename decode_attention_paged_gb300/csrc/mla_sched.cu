@@ -55,7 +55,7 @@ __device__ __forceinline__ int last_le(const int32_t* C, int n, int64_t x) {
 }
 
 __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ seqlens,
-                                                   int uniform_len, int batch, int R,
+                                                   int seq_div, int uniform_len, int batch, int R,
                                                    int num_parts, int n_mtiles, int fixed,
                                                    int32_t* meta, int32_t* num_splits) {
     // Let the decode kernel (programmatically dependent) run its prologue now;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ s
     int carry = 0;
     for (int base = 0; base < batch; base += 32) {
         const int i = base + lane;
-        const int32_t L = seqlens ? (i < batch ? seqlens[i] : 0) : uniform_len;
+        const int32_t L = seqlens ? (i < batch ? seqlens[i / seq_div] : 0) : uniform_len;
         const int v = i < batch ? static_cast<int>(blocks_of(L)) + c : 0;
         const int incl = warp_inclusive_scan(v);
         if (i < batch) C[i + 1] = carry + incl;
@@ -151,9 +151,9 @@ __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ s
 
 int sched_max_batch() { return kSchedMaxBatch; }
 
-cudaError_t launch_sched(const int32_t* seqlens, int uniform_len, int batch, int R, int num_parts,
-                         int n_mtiles, int fixed_overhead, int32_t* meta, int32_t* num_splits,
-                         cudaStream_t stream) {
+cudaError_t launch_sched(const int32_t* seqlens, int seq_div, int uniform_len, int batch, int R,
+                         int num_parts, int n_mtiles, int fixed_overhead, int32_t* meta,
+                         int32_t* num_splits, cudaStream_t stream) {
     const size_t smem = 2 * sizeof(int32_t) * (static_cast<size_t>(batch) + 1);
     // Same shared-memory carveout as the decode kernels, so that a step's
     // kernels follow one another without reconfiguring the SMs.
@@ -173,8 +173,8 @@ cudaError_t launch_sched(const int32_t* seqlens, int uniform_len, int batch, int
                                              static_cast<int>(2 * sizeof(int32_t) * (kSchedMaxBatch + 1)));
         if (e != cudaSuccess) return e;
     }
-    sched_kernel<<<1, 32, smem, stream>>>(seqlens, uniform_len, batch, R, num_parts, n_mtiles,
-                                          fixed_overhead, meta, num_splits);
+    sched_kernel<<<1, 32, smem, stream>>>(seqlens, seq_div < 1 ? 1 : seq_div, uniform_len, batch, R,
+                                          num_parts, n_mtiles, fixed_overhead, meta, num_splits);
     return cudaGetLastError();
 }
 

@@ -35,9 +35,17 @@
  *     block-table row, metadata built for another shape, a pipeline wait that
  *     exceeded its time budget) are recorded in a per-device error word and
  *     reported by mla_last_device_error().
- * Supported: bf16 q / k_cache / out, fp32 lse, h_kv = 1, d_qk = 576,
- * d_v = 512, page size 64, batch <= 16384, GPUs of compute capability 10.3
- * (GB300); other shapes return MLA_ERR_UNSUPPORTED.
+ * Supported: bf16 q / k_cache / out, fp32 lse, d_qk = 576, d_v = 512, page
+ * size 64, batch * h_kv <= 16384, GPUs of compute capability 10.3 (GB300);
+ * other shapes return MLA_ERR_UNSUPPORTED.
+ *
+ * Several cache heads (h_kv > 1; "[DeepSeek-3] FlashMLA", sec. 4: k_cache is
+ * [blocks, 64, h_kv, 576] and the dense tests cover MQA and GQA): query heads
+ * j*g .. j*g+g-1 (g = h_q / h_kv) attend to cache head j, each group as in the
+ * definition above.  h_q must be a multiple of h_kv, and g must divide 64 or
+ * be a multiple of 64 (else MLA_ERR_UNSUPPORTED); the heads of a token are
+ * adjacent in the cache (head stride 576).  Not with MLA_KERNEL_PAIR, sparse
+ * decode or the FP8 layout (MLA_ERR_UNSUPPORTED).
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -86,11 +94,14 @@ MLA_API int mla_version(void);
  * Source: "FlashMLA 新内核深度解析", section "Tile Scheduler" (DecodingSchedMeta
  * per SM part, num_splits per request).
  *   meta_bytes: int32 header[8] + num_sm_parts records of 8 int32 each, where
- *     num_sm_parts = max(1, SMs / ceil(s_q*h_q / 64)) on the current device;
+ *     num_sm_parts = max(1, SMs / ceil(s_q*h_q / h_kv / 64)) on the current device;
  *   num_splits_bytes: int32[batch + 1].
+ * With h_kv > 1 the plan's requests are the (request, cache head) pairs:
+ * num_splits is int32[batch * h_kv + 1] and a tile has s_q*h_q/h_kv rows.
  * Either output pointer may be NULL.  Errors: INVALID_ARGUMENT for
- * batch < 1, h_q < 1, s_q < 1; UNSUPPORTED for h_kv != 1; NO_DEVICE / CUDA
- * when the device cannot be queried.
+ * batch < 1, h_q < 1, s_q < 1, h_kv < 1 or h_q not a multiple of h_kv;
+ * UNSUPPORTED for the head groupings above; NO_DEVICE / CUDA when the device
+ * cannot be queried.
  */
 MLA_API int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t *meta_bytes,
                       size_t *num_splits_bytes);
@@ -133,9 +144,10 @@ MLA_API int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t *by
  *                rows are packed (row stride 576, s stride h_q*576 elements);
  *                q_batch_stride (elements) is free but a multiple of 8.
  *                16-byte aligned.
- *   k_cache_dev  bf16 [num_pages][64][h_kv = 1][576]; k_page_stride and
+ *   k_cache_dev  bf16 [num_pages][64][h_kv][576]; k_page_stride and
  *                k_token_stride in elements, multiples of 8, the 576 dims
- *                contiguous.  16-byte aligned.  Slots of the last page of a
+ *                of a head contiguous and the h_kv heads of a token adjacent
+ *                (k_token_stride >= h_kv * 576).  16-byte aligned.  Slots of the last page of a
  *                sequence beyond its length never influence the result.
  *   block_table_dev int32 [batch][max_blocks_per_seq], row stride
  *                bt_batch_stride (elements).  Entries for blocks

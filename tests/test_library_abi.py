@@ -60,7 +60,11 @@ def test_host_side_argument_checks(lib):
     mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.mla_metadata_size(0, 16, 1, 1, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_INVALID_ARGUMENT
     assert lib.mla_metadata_size(1, 0, 1, 1, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_INVALID_ARGUMENT
-    assert lib.mla_metadata_size(1, 16, 1, 2, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_UNSUPPORTED
+    # cache heads: h_q must split into equal groups; a query tile takes whole
+    # groups of 64/g tokens or a 64-head slice, so g divides 64 or 64 divides g
+    assert lib.mla_metadata_size(1, 16, 1, 3, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_INVALID_ARGUMENT
+    assert lib.mla_metadata_size(1, 96, 1, 2, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_UNSUPPORTED
+    assert lib.mla_metadata_size(1, 16, 1, 0, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_INVALID_ARGUMENT
     ws = ctypes.c_size_t()
     assert lib.mla_workspace_size(1, 16, 1, 1, None) == _lib.MLA_ERR_INVALID_ARGUMENT
     assert lib.mla_workspace_size(1, 16, 0, 1, ctypes.byref(ws)) == _lib.MLA_ERR_INVALID_ARGUMENT
@@ -80,6 +84,9 @@ def test_without_gpu_calls_report_no_device(lib):
         pytest.skip("a GPU is present")
     mb, sb = ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.mla_metadata_size(4, 16, 1, 1, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_NO_DEVICE
+    # a valid cache-head split passes the host checks
+    assert lib.mla_metadata_size(4, 16, 2, 2, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_NO_DEVICE
+    assert lib.mla_metadata_size(4, 256, 1, 2, ctypes.byref(mb), ctypes.byref(sb)) == _lib.MLA_ERR_NO_DEVICE
 
 
 def test_sparse_host_side_argument_checks(lib):
