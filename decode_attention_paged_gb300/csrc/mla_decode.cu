@@ -77,11 +77,6 @@ constexpr float kLazyThreshold = 8.0f;  // log2 units (factor 256)
 // own, so the drain has its own budget, independent of the (possibly tiny)
 // wait budget a caller set.
 constexpr uint64_t kDrainBudgetNs = 2000000000ull;
-#ifndef MLA_MMA_STRICT
-#define MLA_MMA_STRICT 0
-#endif
-// 1: QK^T of block g + 1 is issued only after PV of block g.
-constexpr bool kStrictOrder = MLA_MMA_STRICT != 0;
 #ifndef MLA_IDLE_SLEEP_NS
 #define MLA_IDLE_SLEEP_NS 32
 #endif
@@ -489,8 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // probes the barriers without blocking and broadcasts what it saw, and
         // each MMA is issued by one elected lane, so operand descriptors stay
         // warp-uniform (single-thread issue measured ~1.5x slower per MMA).
-        // QK^T goes out three 64-dim chunks (12 MMAs) per turn, with a check
-        // for a ready PV between turns: a PV never waits behind a whole QK^T.
+        // QK^T goes out in one burst of 36 MMAs once its page is in: splitting
+        // it into turns with a check for a ready PV between them (so that a
+        // PV never waits behind a whole QK^T) measured 4-19% slower, because
+        // the checks stretched how long each stage is held.
         constexpr uint32_t idesc_pv = idesc_bf16_f32(64, 256, false, true);
         // Descriptors are built once; an MMA's operand then differs only in
         // the start-address field (bits 0..13, 16-byte units), which a plain
@@ -510,7 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO0 = tmem + kColO, tO1 = tmem + kColO + 128;
         constexpr uint64_t kChunkUnits = kChunkBytes >> 4;
         Cursor qk = cursor_begin<kHeads>(p, part), pv = qk;
-        int qk_chunk = 0;  // next 64-dim chunk of QK^T(qk.g) to issue; 0 = not started
         uint64_t idle_since = 0;
         uint32_t idle_spins = 0;
         const bool leader = lane == 0;
@@ -546,38 +542,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     did = true;
                 }
             }
-            if (qk.valid && (!kStrictOrder || qk.g == pv.g)) {
+            if (qk.valid) {
                 const int st = qk.g & 1;
                 bool ready = true;
-                if (qk_chunk == 0) {
-                    if (leader) {
-                        if (qk.blk == qk.b0) ready = mbar_test_wait(&bars->q_full, qk.item & 1);
-                        ready = ready && mbar_test_wait(&bars->kv_full[st], (qk.g >> 1) & 1);
-                        if (ready && qk.g >= 2)
-                            ready = mbar_test_wait(&bars->s_empty[st], ((qk.g >> 1) + 1) & 1);
-                    }
-                    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-                    if (ready) tc_fence_after();
+                if (leader) {
+                    if (qk.blk == qk.b0) ready = mbar_test_wait(&bars->q_full, qk.item & 1);
+                    ready = ready && mbar_test_wait(&bars->kv_full[st], (qk.g >> 1) & 1);
+                    if (ready && qk.g >= 2)
+                        ready = mbar_test_wait(&bars->s_empty[st], ((qk.g >> 1) + 1) & 1);
                 }
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                 if (ready) {
+                    tc_fence_after();
                     const uint64_t bK = st ? dK1 : dK0;
                     const uint32_t d = st ? tS1 : tS0;
-                    if (qk_chunk == 0)
-                        issue_qk_turn<0>(dQ, bK, d);
-                    else if (qk_chunk == 3)
-                        issue_qk_turn<3>(dQ, bK, d);
-                    else
-                        issue_qk_turn<6>(dQ, bK, d);
-                    qk_chunk += 3;
-                    if (qk_chunk == kChunks) {
-                        qk_chunk = 0;
-                        if (elect_one()) {
-                            mma_commit(&bars->s_full[st]);
-                            if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
-                        }
-                        __syncwarp();
-                        cursor_next<kHeads>(p, part, qk);
+                    issue_qk_turn<0>(dQ, bK, d);
+                    issue_qk_turn<3>(dQ, bK, d);
+                    issue_qk_turn<6>(dQ, bK, d);
+                    if (elect_one()) {
+                        mma_commit(&bars->s_full[st]);
+                        if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
                     }
+                    __syncwarp();
+                    cursor_next<kHeads>(p, part, qk);
                     did = true;
                 }
             }
