@@ -706,9 +706,9 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     p.kv_page_bytes = k_page_stride_bytes;
     p.num_tokens = static_cast<int64_t>(num_pages) * kPage;
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
-    // (The kernel takes a page tensor map too; the FP8 path never reads it.)
     p.kvh = 1;
     p.grp = h_q;
+    // (The kernel takes a page tensor map too; the FP8 path never reads it.)
     cudaError_t e = launch_decode(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R, parts,

@@ -54,8 +54,7 @@
 //     MLA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
 //     returns.  Waits in the softmax warps are taken by lane 0 and broadcast,
 //     so control flow stays warp-uniform.
-#include <cuda_fp8.h>
-
+#include "mla_fp8.cuh"
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -97,11 +96,8 @@ struct Barriers {
 };
 
 // FP8 cache: a page's 64 raw rows of 656 bytes land at the top of its stage
-// and are dequantised in place into the bf16 layout below them.
-constexpr uint32_t kFp8RowBytes = 656;
-constexpr uint32_t kFp8PageBytes = kPage * kFp8RowBytes;  // 41984
-constexpr uint32_t kRawOff = kStageBytes - kFp8PageBytes;  // 31744, 16-byte aligned
-static_assert(kRawOff % 16 == 0 && kFp8PageBytes % 16 == 0, "bulk copy alignment");
+// and are dequantised in place into the bf16 layout below them (mla_fp8.cuh).
+static_assert(kFp8RawOff + kFp8PageBytes == kStageBytes, "raw rows at the top of a stage");
 constexpr uint32_t kDequantBar = 1;  // named barrier of the four dequant warps
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
@@ -413,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         raw_bad[st] = in ? 0 : 1;
                         if (in) {
                             mbar_arrive_expect_tx(&bars->raw_full[st], kFp8PageBytes);
-                            bulk_load(dst + kRawOff,
+                            bulk_load(dst + kFp8RawOff,
                                       p.kv_bytes + static_cast<int64_t>(page) * p.kv_page_bytes,
                                       kFp8PageBytes, &bars->raw_full[st], policy);
                         } else {
@@ -670,60 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (kFp8) {
             // ---------------------------------------- FP8 page dequantisation
-            // Two threads per cached row: thread (t, hh) takes latent dims
-            // [256 hh, 256 hh + 256) with their two scales and RoPE dims
-            // [32 hh, 32 hh + 32).  The raw rows sit in the top of the stage
-            // that the bf16 rows overwrite, so every thread reads all its raw
-            // bytes before any thread writes (a named barrier of these four
-            // warps, whose exits are agreed through bar.red.and).  Each value
-            // becomes bf16(e4m3 * scale): the e4m3 -> f16 conversion is exact,
-            // the product is rounded to fp32, then to bf16 (nearest even).
+            // In place, two threads per row (mla_fp8.cuh); the four warps
+            // agree on every exit through bar.red.and before the named
+            // barrier inside the routine.
             const int dt = tid - 32 * kGatherWarp0;
-            const int t = dt >> 1, hh = dt & 1;
             for (Cursor c = cursor_begin<kHeads>(p, part); c.valid; cursor_next<kHeads>(p, part, c)) {
                 const int st = c.g & 1;
                 const bool ok = warp_wait(&bars->raw_full[st], (c.g >> 1) & 1, wc);
                 if (!named_bar_and(kDequantBar, 128, ok)) break;
-                uint8_t* stage = sKV + st * kStageBytes;
-                const uint8_t* raw = stage + kRawOff + t * kFp8RowBytes;
-                const bool bad = raw_bad[st] != 0;
-                uint4 lat[16], rope[4];
-                float sc[2];
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    lat[u] = *reinterpret_cast<const uint4*>(raw + 256 * hh + 16 * u);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    rope[u] = *reinterpret_cast<const uint4*>(raw + 528 + 64 * hh + 16 * u);
-                sc[0] = *reinterpret_cast<const float*>(raw + 512 + 8 * hh);
-                sc[1] = *reinterpret_cast<const float*>(raw + 516 + 8 * hh);
-                named_bar_sync(kDequantBar, 128);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float s = sc[u >> 3];
-                    const uint32_t in[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
-                    uint32_t o[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const __nv_fp8x2_storage_t two =
-                            static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1)));
-                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-                        o[j] = bad ? 0u : pack_bf16x2(f.x * s, f.y * s);
-                    }
-                    const int dim0 = 256 * hh + 16 * u;  // 16 dims: two 16-byte units
-                    uint8_t* chunk = stage + (dim0 >> 6) * kChunkBytes;
-                    const uint32_t unit = (dim0 & 63) >> 3;
-                    *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit + 1)) =
-                        make_uint4(o[4], o[5], o[6], o[7]);
-                }
-                uint8_t* rchunk = stage + 8 * kChunkBytes;
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4*>(rchunk + sw128_offset(t, 4 * hh + u)) =
-                        bad ? make_uint4(0, 0, 0, 0) : rope[u];
+                fp8_dequant_page(sKV + st * kStageBytes, dt, raw_bad[st] != 0, kDequantBar);
                 fence_proxy_async_smem();
                 warp_arrive(&bars->kv_full[st]);
             }

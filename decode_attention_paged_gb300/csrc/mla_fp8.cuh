@@ -1,0 +1,70 @@
+// mla_fp8.cuh -- in-place dequantisation of one page of the FP8 cache layout
+// ("[DeepSeek-3] FlashMLA：把 MLA 的 KV Cache 优势变成 GPU 吞吐", sec. 12: a row
+// of 656 bytes = 512 float8_e4m3 latent values, 4 fp32 scales each shared by
+// 128 of them, 64 bf16 RoPE values), used by the decode kernels that read it.
+#pragma once
+
+#include <cuda_fp8.h>
+
+#include "sm103_ptx.cuh"
+
+namespace mla {
+
+constexpr uint32_t kFp8RowBytes = 656;
+constexpr uint32_t kFp8PageBytes = 64 * kFp8RowBytes;  // 41984: one bulk copy
+// The raw rows land at the top of a 72 KB stage and are rewritten below them.
+constexpr uint32_t kFp8RawOff = 9 * 8192 - kFp8PageBytes;  // 31744, 16-byte aligned
+static_assert(kFp8RawOff % 16 == 0 && kFp8PageBytes % 16 == 0, "bulk copy alignment");
+
+// Four warps (dt = 0..127 among them) turn the page's raw rows at
+// stage + kFp8RawOff into the bf16 page the MMAs read: 9 chunks of
+// [64 rows x 64 dims], 128-byte swizzled, latent dims in chunks 0..7 and the
+// RoPE in chunk 8.  Two threads per row: thread (t, hh) takes latent dims
+// [256 hh, 256 hh + 256) with their two scales and RoPE dims
+// [32 hh, 32 hh + 32).  The raw rows overlap the bf16 rows, so every thread
+// reads all its raw bytes before any thread writes (named barrier bar_id of
+// the four warps).  Each value becomes bf16(e4m3 * scale): e4m3 -> f16 is
+// exact, the product is rounded to fp32, then to bf16 (nearest even).  A page
+// outside the cache (bad) becomes zeros.  The caller fences the writes for
+// the tensor core and signals the page.
+__device__ __forceinline__ void fp8_dequant_page(uint8_t* stage, int dt, bool bad,
+                                                 uint32_t bar_id) {
+    const int t = dt >> 1, hh = dt & 1;
+    const uint8_t* raw = stage + kFp8RawOff + t * kFp8RowBytes;
+    uint4 lat[16], rope[4];
+    float sc[2];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) lat[u] = *reinterpret_cast<const uint4*>(raw + 256 * hh + 16 * u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) rope[u] = *reinterpret_cast<const uint4*>(raw + 528 + 64 * hh + 16 * u);
+    sc[0] = *reinterpret_cast<const float*>(raw + 512 + 8 * hh);
+    sc[1] = *reinterpret_cast<const float*>(raw + 516 + 8 * hh);
+    named_bar_sync(bar_id, 128);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const float s = sc[u >> 3];
+        const uint32_t in[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __nv_fp8x2_storage_t two =
+                static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1)));
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            o[j] = bad ? 0u : pack_bf16x2(f.x * s, f.y * s);
+        }
+        const int dim0 = 256 * hh + 16 * u;  // 16 dims: two 16-byte units
+        uint8_t* chunk = stage + (dim0 >> 6) * 8192;
+        const uint32_t unit = (dim0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit + 1)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    uint8_t* rchunk = stage + 8 * 8192;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(rchunk + sw128_offset(t, 4 * hh + u)) =
+            bad ? make_uint4(0, 0, 0, 0) : rope[u];
+}
+
+}  // namespace mla
