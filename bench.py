@@ -71,6 +71,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, dist=None):
+    """The slowest rank's value, on every rank (the timing rule for N > 1)."""
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_workload(W_mod, name, rank):
+    """Weak scaling: every rank decodes its own seeded batch of the workload."""
+    return W_mod.CONFIGS[name](seed_offset=1000 * rank)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -472,7 +487,7 @@ def main():
                            "tq": api.KERNEL_TQ}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     # weak scaling: every rank decodes its own batch of requests (replicas).
-    w = W_mod.CONFIGS[args.workload](seed_offset=1000 * rank)
+    w = replica_workload(W_mod, args.workload, rank)
     sampler = ClockSampler(list(range(world)) if world > 1 else [local]) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -480,10 +495,7 @@ def main():
     if sampler:
         sampler.stop()
 
-    t = torch.tensor([res["ms_total"]], dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total = float(t.item())
+    ms_total = max_over_ranks(res["ms_total"], dist)
     ms_step = ms_total / args.steps
     gbs = res["bytes"] * world / (ms_step * 1e-3) / 1e9
     tflops = res["flops"] * world / (ms_step * 1e-3) / 1e12
