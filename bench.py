@@ -563,6 +563,26 @@ def main():
         }
         del wf
         torch.cuda.empty_cache()
+        wh = W_mod.gqa()
+        kx = max(50, min(args.steps, 1000))
+        gh = wh.to("cuda")
+        meta_h, ns_h = api.mla_get_metadata(gh.cache_seqlens, wh.h_q, wh.s_q, wh.h_kv)
+        call_h = api.DecodeCall(gh.q, gh.k_cache, gh.block_table, gh.cache_seqlens,
+                                wh.softmax_scale, wh.causal, meta_h, ns_h)
+        gr_h = capture(torch, call_h.fwd)
+        ms_h, _ = time_steps(torch, gr_h, kx, 5)
+        assert api.mla_last_device_error() == 0
+        t_s = ms_h / kx * 1e-3
+        sl = wh.cache_seqlens.tolist()
+        bytes_h = W_mod.heads_hbm_bytes(sl, wh.s_q, wh.h_q, wh.h_kv)
+        flops_h = W_mod.flops(sl, wh.s_q, wh.h_q, wh.causal)
+        extra["gqa"] = {
+            "workload": wh.name, "ms_per_step": ms_h / kx,
+            "step_gbs": bytes_h / t_s / 1e9, "step_tflops": flops_h / t_s / 1e12,
+            "frac_hbm_peak": bytes_h / t_s / 1e9 / hbm_peak, "steps": kx,
+        }
+        del gr_h, call_h, gh, wh
+        torch.cuda.empty_cache()
         ws = W_mod.sparse()
         kx = max(50, min(args.steps, 1000))
         r = measure_sparse(ws, torch, api, W_mod, kx, 5)

@@ -320,3 +320,56 @@ def fp8_hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int) -> int:
     plus q in, out and lse out."""
     rows = len(seqlens) * s_q * h_q
     return sum(int(L) for L in seqlens) * FP8_ROW_BYTES + rows * (D_QK * 2 + D_V * 2 + 4)
+
+
+# ------------------------------------------------------------ h_kv > 1
+@dataclasses.dataclass
+class HeadsWorkload:
+    """Decode with several cache heads: k_cache [pages, 64, h_kv, 576]."""
+    name: str
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    block_table: torch.Tensor
+    cache_seqlens: torch.Tensor
+    softmax_scale: float
+    causal: bool
+
+    @property
+    def b(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def s_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def h_q(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def h_kv(self) -> int:
+        return self.k_cache.shape[2]
+
+    def to(self, device) -> "HeadsWorkload":
+        return dataclasses.replace(
+            self, q=self.q.to(device), k_cache=self.k_cache.to(device),
+            block_table=self.block_table.to(device), cache_seqlens=self.cache_seqlens.to(device))
+
+
+def gqa(seed_offset: int = 0) -> HeadsWorkload:
+    """batch 32, s_q 1, h_q 64, h_kv 4 (groups of 16 heads), every L = 4096,
+    2048 pages permuted: 604 MB of cache."""
+    b, h_q, h_kv, L = 32, 64, 4, 4096
+    nb = L // PAGE
+    perm = torch.randperm(b * nb, generator=_gen(3 + seed_offset)).to(torch.int32)
+    bt = perm.view(b, nb).contiguous()
+    q = _randn_bf16((b, 1, h_q, D_QK), 1 + seed_offset)
+    kc = _randn_bf16((b * nb, PAGE, h_kv, D_QK), 2 + seed_offset)
+    return HeadsWorkload("GQA b32 s_q1 h_q64 h_kv4 L4096", q, kc, bt,
+                         torch.full((b,), L, dtype=torch.int32), SCALE, False)
+
+
+def heads_hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int, h_kv: int) -> int:
+    """Algorithmic bytes with h_kv cache heads: 1152 B per cached token and head."""
+    rows = len(seqlens) * s_q * h_q
+    return sum(int(L) for L in seqlens) * h_kv * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)
