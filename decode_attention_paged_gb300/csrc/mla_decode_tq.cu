@@ -446,6 +446,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* v_slot = reinterpret_cast<float*>(smem + lay.off_v);  // [128] row max / row sum
         uint32_t gblk = 0, item = 0;
         bool alive = true;
+        // Q tile of a request, from its ring stage (ring entry nq): dims
+        // 0..447 into this lane's TMEM copy, dims 448..575 into the packed
+        // chunks (by the lane group 0 threads; both groups hold the same rows).
+        // Needs only the previous request's QK^T to be complete, so it runs
+        // before that request's epilogue and the next QK^T overlaps the
+        // epilogue.
+        auto q_copy = [&](uint32_t nq) -> bool {
+            const uint32_t stq = nq % n_stages;
+            if (!named_bar_and(pair_bar, 64, warp_wait(&bars->kv_full[stq], (nq / n_stages) & 1, wc)))
+                return false;
+            const uint8_t* sq = sKV + stq * kStageBytes;
+            const bool have = r < p.q_box_rows;
+#pragma unroll 1
+            for (int c = 0; c < kTmemChunks; ++c) {
+                uint32_t w[32];
+                if (have) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        ld_shared_v4(smem_u32(sq + c * kChunkBytes + sw128_offset(r, u)), w[4 * u],
+                                     w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = 0u;
+                }
+                tmem_st32(tl + kColQ + 32 * c, w);
+            }
+            if (half == 0 && r < static_cast<int>(lay.q_rows)) {
+                // rows keep their 128-byte swizzle: both bases are 1024-aligned
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            sq + (kTmemChunks + i) * kChunkBytes + r * 128 + u * 16);
+                        *reinterpret_cast<uint4*>(sQr + i * lay.q_rows * 128 + r * 128 + u * 16) = v;
+                    }
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&bars->q_ready);
+            return true;
+        };
+        int q_done = -1;  // request whose Q tile is already in place
         for (int req = part.begin_req; req <= part.end_req && alive; ++req) {
             int L, nb, b0, b1;
             item_range(p, part, req, L, nb, b0, b1);
@@ -458,49 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool split = (p.num_splits[req + 1] - first_piece) > 1;
             const int slot = (req == part.begin_req) ? part.begin_split : first_piece;
             const bool has_blocks = b1 > b0;
-            if (has_blocks) {
-                // Q tile of this request, from its ring stage: dims 0..447 into
-                // this lane's TMEM copy, dims 448..575 into the packed chunks
-                // (by the lane group 0 threads; both groups hold the same rows).
-                const uint32_t nq = gblk + item;
-                const uint32_t stq = nq % n_stages;
-                if (!named_bar_and(pair_bar, 64,
-                                   warp_wait(&bars->kv_full[stq], (nq / n_stages) & 1, wc))) {
+            if (has_blocks && q_done != req) {
+                if (!q_copy(gblk + item)) {
                     alive = false;
                     break;
                 }
-                const uint8_t* sq = sKV + stq * kStageBytes;
-                const bool have = r < p.q_box_rows;
-#pragma unroll 1
-                for (int c = 0; c < kTmemChunks; ++c) {
-                    uint32_t w[32];
-                    if (have) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            ld_shared_v4(smem_u32(sq + c * kChunkBytes + sw128_offset(r, u)),
-                                         w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = 0u;
-                    }
-                    tmem_st32(tl + kColQ + 32 * c, w);
-                }
-                if (half == 0 && r < static_cast<int>(lay.q_rows)) {
-                    // rows keep their 128-byte swizzle: both bases are 1024-aligned
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(
-                                sq + (kTmemChunks + i) * kChunkBytes + r * 128 + u * 16);
-                            *reinterpret_cast<uint4*>(sQr + i * lay.q_rows * 128 + r * 128 + u * 16) =
-                                v;
-                        }
-                }
-                fence_proxy_async_smem();
-                tmem_st_wait();
-                tc_fence_before();
-                warp_arrive(&bars->q_ready);
             }
             float m_used = -INFINITY, l_part = 0.f;
             for (int blk = b0; blk < b1; ++blk, ++gblk) {
@@ -606,6 +612,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 warp_arrive(&bars->p_full[gblk & 1]);
             }
             if (!alive) break;
+            if (has_blocks) {
+                // The next request with blocks: its Q tile (the ring entry
+                // after this request's last page) goes in now.
+                for (int nr = req + 1; nr <= part.end_req; ++nr) {
+                    int L2, nb2, c0, c1;
+                    item_range(p, part, nr, L2, nb2, c0, c1);
+                    if (c1 > c0) {
+                        if (!q_copy(gblk + item + 1)) alive = false;
+                        q_done = nr;
+                        break;
+                    }
+                }
+                if (!alive) break;
+            }
 
             // ---------------------------------------------------- epilogue
             float l_tot = 0.f;
