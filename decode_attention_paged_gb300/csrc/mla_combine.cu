@@ -46,6 +46,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int req = blockIdx.y;
     const int row = blockIdx.x * kCombineWarps + warp;
+    // The next decode grid may launch now: it waits for this grid's completion
+    // before it reads its plan or writes anything.
+    pdl_launch_dependents();
     pdl_wait_primary();
     if (row >= p.R) return;
     // Metadata built for another shape: the decode kernel has already recorded

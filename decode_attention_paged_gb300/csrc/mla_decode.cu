@@ -334,6 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The dependent (combine) grid may launch now: it waits for this grid's
+    // completion before it reads anything (griddepcontrol.wait).
+    pdl_launch_dependents();
 
     // Everything above touched only on-chip state; global inputs may be
     // written by the preceding kernel on the stream (programmatic launch).
@@ -892,7 +895,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ teardown
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
