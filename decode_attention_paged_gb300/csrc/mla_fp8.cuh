@@ -27,6 +27,17 @@ static_assert(kFp8RawOff % 16 == 0 && kFp8PageBytes % 16 == 0, "bulk copy alignm
 // exact, the product is rounded to fp32, then to bf16 (nearest even).  A page
 // outside the cache (bad) becomes zeros.  The caller fences the writes for
 // the tensor core and signals the page.
+// Two fp32 products in one instruction (each lane rounded to nearest, as the
+// scalar multiply), packed to bf16x2.
+__device__ __forceinline__ uint32_t mul2_pack_bf16x2(float x0, float x1, uint64_t s2) {
+    uint64_t x, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(s2));
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(z));
+    return pack_bf16x2(a, b);
+}
+
 __device__ __forceinline__ void fp8_dequant_page(uint8_t* stage, int dt, bool bad,
                                                  uint32_t bar_id) {
     const int t = dt >> 1, hh = dt & 1;
@@ -40,9 +51,12 @@ __device__ __forceinline__ void fp8_dequant_page(uint8_t* stage, int dt, bool ba
     sc[0] = *reinterpret_cast<const float*>(raw + 512 + 8 * hh);
     sc[1] = *reinterpret_cast<const float*>(raw + 516 + 8 * hh);
     named_bar_sync(bar_id, 128);
+    uint64_t s2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        asm("mov.b64 %0, {%1, %1};" : "=l"(s2[h]) : "f"(sc[h]));
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-        const float s = sc[u >> 3];
         const uint32_t in[4] = {lat[u].x, lat[u].y, lat[u].z, lat[u].w};
         uint32_t o[8];
 #pragma unroll
@@ -51,7 +65,7 @@ __device__ __forceinline__ void fp8_dequant_page(uint8_t* stage, int dt, bool ba
                 static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1)));
             const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            o[j] = bad ? 0u : pack_bf16x2(f.x * s, f.y * s);
+            o[j] = bad ? 0u : mul2_pack_bf16x2(f.x, f.y, s2[u >> 3]);
         }
         const int dim0 = 256 * hh + 16 * u;  // 16 dims: two 16-byte units
         uint8_t* chunk = stage + (dim0 >> 6) * 8192;
