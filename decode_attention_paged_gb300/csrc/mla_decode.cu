@@ -736,10 +736,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float x[32];
                 float hmax = -INFINITY;
+                const uint64_t sc2 = f32x2_splat(p.scale_log2);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = ((keys >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-                    hmax = fmaxf(hmax, x[c]);
+                for (int c = 0; c < 32; c += 2) {
+                    float a0, a1;
+                    f32x2_mul(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sc2, a0, a1);
+                    x[c] = ((keys >> c) & 1u) ? a0 : -INFINITY;
+                    x[c + 1] = ((keys >> (c + 1)) & 1u) ? a1 : -INFINITY;
+                    hmax = fmaxf(hmax, fmaxf(x[c], x[c + 1]));
                 }
                 float pmax;
                 if (!pair_exchange(xch, Lrow, xseq, hmax, pmax, wc)) {
@@ -756,16 +760,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (need) l_part *= alpha;
                 uint32_t pk[16];
-                float psum = 0.f;
                 const bool none = (m_used == -INFINITY);
+                const uint64_t m2 = f32x2_splat(m_used);
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = none ? 0.f : fast_exp2(x[2 * c] - m_used);
-                    const float p1 = none ? 0.f : fast_exp2(x[2 * c + 1] - m_used);
-                    psum += p0 + p1;
+                    float d0, d1;
+                    f32x2_sub(x[2 * c], x[2 * c + 1], m2, d0, d1);
+                    const float p0 = none ? 0.f : fast_exp2(d0);
+                    const float p1 = none ? 0.f : fast_exp2(d1);
+                    f32x2_add(ps0, ps1, p0, p1, ps0, ps1);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                l_part += psum;
+                l_part += ps0 + ps1;
 
                 // With P in page g's own RoPE chunk (kStageP), only a
                 // rescale of O has to wait for PV(g - 1); otherwise the wait

@@ -530,11 +530,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t0 = blk * kPage + 32 * half;
                 float x[32];
                 float hmax = -INFINITY;
+                const int nvis = row_valid ? lim - t0 : 0;  // columns c < nvis are visible
+                const uint64_t sc2 = f32x2_splat(p.scale_log2);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = (row_valid && t0 + c < lim) ? __uint_as_float(sv[c]) * p.scale_log2
-                                                       : -INFINITY;
-                    hmax = fmaxf(hmax, x[c]);
+                for (int c = 0; c < 32; c += 2) {
+                    float a0, a1;
+                    f32x2_mul(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sc2, a0, a1);
+                    x[c] = c < nvis ? a0 : -INFINITY;
+                    x[c + 1] = c + 1 < nvis ? a1 : -INFINITY;
+                    hmax = fmaxf(hmax, fmaxf(x[c], x[c + 1]));
                 }
                 // Row max over both halves (the slot is rewritten only after
                 // the next barrier, which the partner passes after reading it).
@@ -550,16 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (need) l_part *= alpha;
                 uint32_t pk[16];
-                float psum = 0.f;
                 const bool none = (m_used == -INFINITY);
+                const uint64_t m2 = f32x2_splat(m_used);
+                float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = none ? 0.f : fast_exp2(x[2 * c] - m_used);
-                    const float p1 = none ? 0.f : fast_exp2(x[2 * c + 1] - m_used);
-                    psum += p0 + p1;
+                    float d0, d1;
+                    f32x2_sub(x[2 * c], x[2 * c + 1], m2, d0, d1);
+                    const float p0 = none ? 0.f : fast_exp2(d0);
+                    const float p1 = none ? 0.f : fast_exp2(d1);
+                    f32x2_add(ps0, ps1, p0, p1, ps0, ps1);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                l_part += psum;
+                l_part += ps0 + ps1;
 
                 // O is rescaled after PV(g - 1).  P has a buffer per stage,
                 // but PV may trail by at most two pages so that the parity

@@ -105,6 +105,35 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint6
     return false;
 }
 
+// ---------------------------------------------------------------- f32x2
+// Packed pairs of fp32 (one instruction for two lanes, each rounded to
+// nearest as the scalar operation).
+__device__ __forceinline__ uint64_t f32x2_splat(float v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ void f32x2_mul(float a0, float a1, uint64_t b, float& o0, float& o1) {
+    uint64_t x, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o0), "=f"(o1) : "l"(z));
+}
+__device__ __forceinline__ void f32x2_sub(float a0, float a1, uint64_t b, float& o0, float& o1) {
+    uint64_t x, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o0), "=f"(o1) : "l"(z));
+}
+__device__ __forceinline__ void f32x2_add(float a0, float a1, float b0, float b1, float& o0,
+                                          float& o1) {
+    uint64_t x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o0), "=f"(o1) : "l"(z));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
