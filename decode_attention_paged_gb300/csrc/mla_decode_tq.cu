@@ -532,13 +532,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float hmax = -INFINITY;
                 const int nvis = row_valid ? lim - t0 : 0;  // columns c < nvis are visible
                 const uint64_t sc2 = f32x2_splat(p.scale_log2);
+                // Pages every valid row of the warp sees whole skip the masking.
+                // (Rows past the tile then hold scores of padding query rows:
+                // they only feed their own output rows, which are never
+                // written, and are left out of the rescale vote.)
+                if (__all_sync(0xffffffffu, !row_valid || nvis >= 32)) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float a0, a1;
-                    f32x2_mul(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sc2, a0, a1);
-                    x[c] = c < nvis ? a0 : -INFINITY;
-                    x[c + 1] = c + 1 < nvis ? a1 : -INFINITY;
-                    hmax = fmaxf(hmax, fmaxf(x[c], x[c + 1]));
+                    for (int c = 0; c < 32; c += 2) {
+                        f32x2_mul(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sc2, x[c],
+                                  x[c + 1]);
+                        hmax = fmaxf(hmax, fmaxf(x[c], x[c + 1]));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float a0, a1;
+                        f32x2_mul(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sc2, a0, a1);
+                        x[c] = c < nvis ? a0 : -INFINITY;
+                        x[c + 1] = c + 1 < nvis ? a1 : -INFINITY;
+                        hmax = fmaxf(hmax, fmaxf(x[c], x[c + 1]));
+                    }
                 }
                 // Row max over both halves (the slot is rewritten only after
                 // the next barrier, which the partner passes after reading it).
@@ -554,15 +567,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (need) l_part *= alpha;
                 uint32_t pk[16];
-                const bool none = (m_used == -INFINITY);
-                const uint64_t m2 = f32x2_splat(m_used);
+                // A row with no visible key yet has only -inf scores: with 0
+                // in place of the -inf max every exp2 is exactly 0.
+                const uint64_t m2 = f32x2_splat(m_used == -INFINITY ? 0.f : m_used);
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     float d0, d1;
                     f32x2_sub(x[2 * c], x[2 * c + 1], m2, d0, d1);
-                    const float p0 = none ? 0.f : fast_exp2(d0);
-                    const float p1 = none ? 0.f : fast_exp2(d1);
+                    const float p0 = fast_exp2(d0);
+                    const float p1 = fast_exp2(d1);
                     f32x2_add(ps0, ps1, p0, p1, ps0, ps1);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
@@ -573,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // waits on the two p_full / pv_done barriers stay unambiguous.
                 // (The two warps of a pair see the same rows, hence the same
                 // rescale decision.)
-                const bool rescale = __any_sync(0xffffffffu, need && blk > b0);
+                const bool rescale = __any_sync(0xffffffffu, need && row_valid && blk > b0);
                 const uint32_t lag = rescale ? 1u : 2u;
                 bool ok = true;
                 if (gblk >= lag) {
