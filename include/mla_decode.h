@@ -164,6 +164,13 @@ MLA_API int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t *by
  *   lse_dev      fp32 [batch][h_q][s_q], contiguous.
  * Enqueues the decode kernel and (programmatically dependent) the combine
  * kernel on `stream`.  Graph-capturable: no allocation, no synchronisation.
+ * Programmatic dependent launch ("FlashMLA 新内核深度解析", section
+ * "Programmatic Dependent Launch"): each kernel lets the next kernel on the
+ * stream launch right after its own prologue, and waits for the previous one
+ * (griddepcontrol.wait) before it reads its inputs or writes anything.  A
+ * caller's kernel launched after this call with the programmatic-serialization
+ * attribute must likewise wait (cudaGridDependencySynchronize) before it reads
+ * out or lse; kernels launched without that attribute are ordered as usual.
  */
 MLA_API int mla_decode_fwd(const void *q_dev, int64_t q_batch_stride, const void *k_cache_dev,
                    int64_t k_page_stride, int64_t k_token_stride, int num_pages, int page_size,
