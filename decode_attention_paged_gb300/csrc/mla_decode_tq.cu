@@ -173,12 +173,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     __syncwarp();
     return ok;
 }
+// The arrive releases (CTA scope) what lane 0 has seen, and the warp barrier
+// orders the other lanes' writes before it.
 __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-        __threadfence_block();
-        mbar_arrive(bar);
-    }
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -381,19 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qk.g >= 1 && !warp_wait(&bars->s_empty, (qk.g - 1) & 1, wc)) break;
             tc_fence_after();
             const uint64_t bK = dK0 + st * kStageUnits;
+            // One elected thread issues the whole burst and commits it.
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 4 * kTmemChunks; ++j)
-                if (elect_one())
+                for (int j = 0; j < 4 * kTmemChunks; ++j)
                     mma_ws_ts(tS, tQ + 8 * j, bK + (j / 4) * kChunkUnits + 2 * (j & 3), idesc_qk,
                               j ? 1u : 0u);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int c = kTmemChunks + j / 4;  // 7, 8
-                if (elect_one())
+                for (int j = 0; j < 8; ++j) {
+                    const int c = kTmemChunks + j / 4;  // 7, 8
                     mma_ws_ss(tS, dQr + (j / 4) * q_chunk_units + 2 * (j & 3),
                               bK + c * kChunkUnits + 2 * (j & 3), idesc_qk, 1u);
+                }
+                mma_commit(&bars->s_full);
             }
-            if (elect_one()) mma_commit(&bars->s_full);
             __syncwarp();
         }
         if (elect_one()) mma_commit(&bars->drain_qk);
