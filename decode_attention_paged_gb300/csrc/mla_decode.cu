@@ -185,12 +185,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return ok;
 }
 // One arrival per warp, after every lane's prior writes.
+// The arrive releases (CTA scope) what lane 0 has seen, and the warp barrier
+// orders the other lanes' writes before it.
 __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-        __threadfence_block();
-        mbar_arrive(bar);
-    }
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // Exchange one float with the partner thread that holds the other half of
@@ -241,8 +240,9 @@ __device__ __forceinline__ bool pair_exchange(uint2* xch, int lrow, uint32_t& se
     return __all_sync(0xffffffffu, ok);
 }
 
-// Chunks [C0, C0 + 3) of S = Q K^T for one page: 12 MMAs, each issued by one
-// elected lane of the converged warp, operand offsets known at compile time.
+// Chunks [C0, C0 + 3) of S = Q K^T for one page: 12 MMAs, issued by the one
+// elected thread that issues the whole burst, operand offsets known at compile
+// time.
 template <int C0>
 __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t d) {
     constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
@@ -251,9 +251,8 @@ __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t
     for (int cc = 0; cc < 3; ++cc) {
         const uint64_t a = dQ + (C0 + cc) * kChunkUnits, b = bK + (C0 + cc) * kChunkUnits;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            if (elect_one()) mma_ws_ss(d, a + 2 * kk, b + 2 * kk, idesc_qk, (C0 + cc + kk) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ws_ss(d, a + 2 * kk, b + 2 * kk, idesc_qk, (C0 + cc + kk) ? 1u : 0u);
     }
 }
 
@@ -525,14 +524,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bV = (pv.g & 1) ? dV1 : dV0;
                     const uint64_t dP = (pv.g & 1) ? dP1 : dP0;
                     const uint32_t acc0 = first ? 0u : 1u;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t acc = kk ? 1u : acc0;
-                        if (elect_one()) mma_ws_ss(tO0, dP + 2 * kk, bV + 128 * kk, idesc_pv, acc);
-                        if (elect_one())
-                            mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk, idesc_pv, acc);
-                    }
+                    // One elected thread issues the burst and commits it.
                     if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t acc = kk ? 1u : acc0;
+                            mma_ws_ss(tO0, dP + 2 * kk, bV + 128 * kk, idesc_pv, acc);
+                            mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk, idesc_pv, acc);
+                        }
                         mma_commit(&bars->pv_done[pv.g & 1]);
                         mma_commit(&bars->kv_empty[pv.g & 1]);
                     }
@@ -555,10 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t bK = st ? dK1 : dK0;
                     const uint32_t d = st ? tS1 : tS0;
-                    issue_qk_turn<0>(dQ, bK, d);
-                    issue_qk_turn<3>(dQ, bK, d);
-                    issue_qk_turn<6>(dQ, bK, d);
                     if (elect_one()) {
+                        issue_qk_turn<0>(dQ, bK, d);
+                        issue_qk_turn<3>(dQ, bK, d);
+                        issue_qk_turn<6>(dQ, bK, d);
                         mma_commit(&bars->s_full[st]);
                         if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
                     }
