@@ -28,7 +28,7 @@
 //     tokens 32..63, so a row's max is combined from two threads.
 //   - Warp roles: warp 0 = TMA producer (lane 0 issues; the warp's lanes
 //     keep block-table entries loaded 32 pages ahead), warp 1 = TMEM owner
-//     and MMA issuer (converged warp, elect.sync), warps 2..5 = softmax /
+//     and MMA issuer (converged warp, one elected thread per burst), warps 2..5 = softmax /
 //     correction / epilogue (one thread per TMEM lane), warps 6..9 = row
 //     gather for sparse decode (idle in dense decode).
 //   - P of a page goes either into that page's RoPE chunk, dead once its
@@ -480,8 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (and, on a request's first block, O released by the previous
         // request's epilogue).  The whole warp runs this loop in step: lane 0
         // probes the barriers without blocking and broadcasts what it saw, and
-        // each MMA is issued by one elected lane, so operand descriptors stay
-        // warp-uniform (single-thread issue measured ~1.5x slower per MMA).
+        // one elected thread issues each burst and its commits.  (An isolated
+        // probe had found single-thread issue ~1.5x slower per MMA than one
+        // elect.sync per MMA; in the kernel, bursts under one elect measured
+        // faster.)
         // QK^T goes out in one burst of 36 MMAs once its page is in: splitting
         // it into turns with a check for a ready PV between them (so that a
         // PV never waits behind a whole QK^T) measured 4-19% slower, because
