@@ -1,17 +1,25 @@
 #!/usr/bin/env python
 """Benchmark of the paged MLA decode path on GB300.
 
-One step = the whole hot path on one batch: mla_get_metadata (tile scheduler)
--> split-KV decode kernel -> combine kernel, through the C ABI.  The headline
+One step = one mla_decode_fwd call on one batch through the C ABI: the
+split-KV decode kernel and the combine kernel.  The plan (mla_get_metadata, the
+tile scheduler) is built once per decode step and shared by every layer, so it
+is built before the timed region and its own duration is reported beside the
+step (kernel_ms.sched); the e2e figure includes it.  The headline
 workload is the memory-bound decode (batch 64, s_q 1, h_q 16, every sequence
 4096 tokens, 64-token pages permuted at random, bf16); metric and unit follow
 the benchmark's definition (TFLOP/s and HBM GB/s of algorithmic work, as a
 fraction of the measured BF16 / HBM peaks).
 
 Timing (rank-local, then max over ranks):
-  * timed region: K replays of a CUDA graph holding one step exactly as a user
-    calls it (programmatic launch between the kernels intact), bracketed by a
-    barrier and a device synchronisation; CUDA events on the replay stream;
+  * timed region (`value`): K back-to-back replays of a CUDA graph holding one
+    step exactly as a user calls it (programmatic launch between the kernels
+    intact), bracketed by a barrier and a device synchronisation; CUDA events
+    on the replay stream.  No L2 flush between replays: the inputs (~300 MB of
+    KV pages) exceed the 129 MB L2;
+  * flushed step: up to 2000 replays of the same graph, each preceded by a
+    write of twice the L2 size outside the events, so that every step starts
+    with a cold L2 (`step_l2_flushed`);
   * kernel region: K steps (at most 2000) with the three kernels launched as
     separate graphs and CUDA events between them, giving each kernel's average
     duration; the decode kernel's inputs exceed L2 (the KV pages alone are
@@ -58,9 +66,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel", choices=["auto", "single", "pair", "tq"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "single", "tq"], default="auto",
                     help="decode kernel: auto (default: tq for s_q*h_q <= 32, else single), "
-                         "single CTA, 2-CTA cluster pair, or Q in TMEM")
+                         "single CTA, or Q in TMEM")
     return ap.parse_args()
 
 
@@ -96,8 +104,7 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-KERNEL_SOURCES = {"pair": ("decode_pair_kernel", "decode_attention_paged_gb300/csrc/mla_decode_pair.cu"),
-                  "single": ("decode_kernel", "decode_attention_paged_gb300/csrc/mla_decode.cu"),
+KERNEL_SOURCES = {"single": ("decode_kernel", "decode_attention_paged_gb300/csrc/mla_decode.cu"),
                   "tq": ("decode_tq_kernel", "decode_attention_paged_gb300/csrc/mla_decode_tq.cu")}
 
 
@@ -196,6 +203,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def kernel_of(kind, w):
+    """Name of the decode kernel a dense call on workload w launches."""
+    if kind != "auto":
+        return kind
+    return "tq" if w.s_q * w.h_q <= 32 else "single"
+
+
+def roofline_of(res, workload, kname, peaks):
+    """Roofline object of the decode kernel of one workload: bound by the
+    side of the ridge its arithmetic intensity falls on; achieved algorithmic
+    bytes (or FLOPs) per launch over the kernel's mean CUDA-event duration."""
+    hbm_peak, bf16_peak, _, peak_src = peaks
+    dec_s = res["ms_decode"] * 1e-3
+    tensor = res["flops"] / res["bytes"] > bf16_peak * 1e12 / (hbm_peak * 1e9)
+    gbs = res["bytes"] / dec_s / 1e9
+    tfl = res["flops"] / dec_s / 1e12
+    r = {"bound": "tensor" if tensor else "hbm",
+         "achieved": tfl if tensor else gbs, "peak": bf16_peak if tensor else hbm_peak,
+         "unit": "TFLOP/s" if tensor else "GB/s",
+         "frac": tfl / bf16_peak if tensor else gbs / hbm_peak,
+         "traffic": profile_traffic(workload, kname),
+         "kernel": KERNEL_SOURCES[kname][0] + " (split-KV)", "peak_source": peak_src,
+         "algorithmic_bytes": res["bytes"], "algorithmic_flops": res["flops"],
+         "hbm_frac": gbs / hbm_peak, "tensor_frac_of_bf16_peak": tfl / bf16_peak,
+         "ms_per_launch": res["ms_decode"], "launches_timed": res["kernel_steps"]}
+    return r
+
+
 # ------------------------------------------------------------------ GPU arm
 def build_step(w, torch, api):
     """Device buffers and the three per-kernel callables of one step."""
@@ -245,6 +280,20 @@ def time_steps(torch, graph, K, W, dist=None):
     return e0.elapsed_time(e1), (t0, t1)
 
 
+def time_steps_flushed(torch, graph, K, flush_buf):
+    """Average duration (ms) of one replay of `graph` when L2 is cold: each
+    replay is preceded by a write of flush_buf, outside the events."""
+    K = max(1, min(K, 2000))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush_buf.add_(1)
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return sum(e[0].elapsed_time(e[1]) for e in ev) / K
+
+
 def time_kernels(torch, g_sched, g_split, g_comb, K, flush_buf):
     """Average duration (ms) of each kernel over K steps, from events placed
     between separately launched single-kernel graphs."""
@@ -287,11 +336,12 @@ def measure_workload(w, torch, api, W_mod, K, Wup, dist=None):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     flush.zero_()
     kt, k_used, win2 = time_kernels(torch, gr_sched, gr_split, gr_comb, K, flush)
+    ms_flushed = time_steps_flushed(torch, gr_full, K, flush)
     code = api.mla_last_device_error()
     assert code == 0, f"device error {code}"
     seqlens = w.cache_seqlens.tolist()
     res = {
-        "ms_total": ms_total, "ms_per_step": ms_total / K,
+        "ms_total": ms_total, "ms_per_step": ms_total / K, "ms_per_step_flushed": ms_flushed,
         "ms_sched": kt[0], "ms_decode": kt[1], "ms_combine": kt[2], "kernel_steps": k_used,
         "flops": W_mod.flops(seqlens, w.s_q, w.h_q, w.causal),
         "bytes": W_mod.hbm_bytes(seqlens, w.s_q, w.h_q),
@@ -399,11 +449,12 @@ def oracle_throughput(w, seconds, W_mod, max_units=None):
     t0 = time.time()
     oracle.mla_decode_rows(p, units_all[:n_run], nthreads=cores)
     dt = time.time() - t0
-    frac = n_run / total_units
-    seqlens = w.cache_seqlens.tolist()
-    gbs = W_mod.hbm_bytes(seqlens, w.s_q, w.h_q) * frac / dt / 1e9
-    tfl = W_mod.flops(seqlens, w.s_q, w.h_q, w.causal) * frac / dt / 1e12
-    sample = f"{n_run} of {total_units} (request, row) units, random order, {dt:.1f} s"
+    nbytes, nflops = W_mod.unit_work(w.cache_seqlens.tolist(), w.s_q, w.h_q, w.causal,
+                                     units_all[:n_run])
+    gbs = nbytes / dt / 1e9
+    tfl = nflops / dt / 1e12
+    sample = (f"{n_run} of {total_units} (request, row) units in a seeded random order, "
+              f"{dt:.1f} s; bytes and FLOPs of exactly those rows")
     return gbs, tfl, cores, sample, dt
 
 
@@ -422,7 +473,12 @@ def reference_arm(args, rank, world):
                        w.cache_seqlens.numpy(), w.softmax_scale, w.causal)
     R = w.s_q * w.h_q
     total_units = w.b * R
-    units_all = np.stack([np.arange(total_units) // R, np.arange(total_units) % R], 1).astype(np.int32)
+    # the seeded random order of oracle_throughput: every step's rows are a
+    # representative mix of the workload's requests, and the work counted is
+    # that of exactly the rows computed
+    order = np.random.default_rng(0).permutation(total_units)
+    units_all = np.stack([order // R, order % R], axis=1).astype(np.int32)
+    seqlens = w.cache_seqlens.tolist()
     t0 = time.time()
     oracle.mla_decode_rows(p, units_all[:cores], nthreads=cores)
     t_batch = max(time.time() - t0, 1e-6)
@@ -432,15 +488,19 @@ def reference_arm(args, rank, world):
     n_step = min(total_units, cores * batches)
     for i in range(args.warmup):
         oracle.mla_decode_rows(p, units_all[:n_step], nthreads=cores)
-    t0 = time.time()
+    nbytes = nflops = 0.0
+    t_run = 0.0
     for i in range(args.steps):
         s = (i * n_step) % total_units
         idx = np.arange(s, s + n_step) % total_units
+        t0 = time.time()
         oracle.mla_decode_rows(p, units_all[idx], nthreads=cores)
-    dt = time.time() - t0
-    frac = n_step / total_units
-    seqlens = w.cache_seqlens.tolist()
-    gbs = W_mod.hbm_bytes(seqlens, w.s_q, w.h_q) * frac * args.steps / dt / 1e9
+        t_run += time.time() - t0
+        b_i, f_i = W_mod.unit_work(seqlens, w.s_q, w.h_q, w.causal, units_all[idx])
+        nbytes += b_i
+        nflops += f_i
+    dt = t_run
+    gbs = nbytes / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -449,9 +509,10 @@ def reference_arm(args, rank, world):
         "config": {"workload": w.name, "batch": w.b, "s_q": w.s_q, "h_q": w.h_q,
                    "page": 64, "parallelism": "host cores"},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n_step} of {total_units} (request, row) units per step"},
+                         "sample": f"{n_step} of {total_units} (request, row) units per step, "
+                                   "seeded random order; bytes and FLOPs of those rows"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "tflops": W_mod.flops(seqlens, w.s_q, w.h_q, w.causal) * frac * args.steps / dt / 1e12,
+        "tflops": nflops / dt / 1e12,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -483,7 +544,6 @@ def main():
     from decode_attention_paged_gb300 import workloads as W_mod
 
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "single": api.KERNEL_SINGLE,
-                           "pair": api.KERNEL_PAIR,
                            "tq": api.KERNEL_TQ}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     # weak scaling: every rank decodes its own batch of requests (replicas).
@@ -514,15 +574,12 @@ def main():
         return 0
 
     clocks = sampler.summary() if sampler else None
-    dec_ms = res["ms_decode"]
-    achieved = res["bytes"] / (dec_ms * 1e-3) / 1e9
-    kname = args.kernel if args.kernel != "auto" else ("tq" if w.s_q * w.h_q <= 32 else "single")
-    traffic = profile_traffic(args.workload, kname)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": KERNEL_SOURCES[kname][0] + " (split-KV)", "peak_source": peak_src,
-                "tensor_frac_of_bf16_peak": res["flops"] / (dec_ms * 1e-3) / 1e12 / bf16_peak,
-                "ms_per_launch": dec_ms, "launches_timed": res["kernel_steps"]}
+    peaks = (hbm_peak, bf16_peak, bf16_sust, peak_src)
+    roofline = roofline_of(res, args.workload, kernel_of(args.kernel, w), peaks)
+    flushed = {"ms_per_step": res["ms_per_step_flushed"],
+               "value": res["bytes"] / (res["ms_per_step_flushed"] * 1e-3) / 1e9, "unit": "GB/s",
+               "what": "mean of up to 2000 replays of the step graph, each after a 2x L2 write "
+                       "outside the events (rank 0)"}
 
     cpu = None
     if world == 1 and not args.no_cpu:
@@ -540,7 +597,9 @@ def main():
             kx = max(50, min(args.steps, 1000))
             r, (gx, cx) = measure_workload(wx, torch, api, W_mod, kx, 5)
             extra[name] = {
-                "ms_per_step": r["ms_per_step"], "ms_decode": r["ms_decode"],
+                "workload": wx.name,
+                "ms_per_step": r["ms_per_step"], "ms_per_step_flushed": r["ms_per_step_flushed"],
+                "ms_decode": r["ms_decode"],
                 "ms_combine": r["ms_combine"], "ms_sched": r["ms_sched"],
                 "decode_tflops": r["flops"] / (r["ms_decode"] * 1e-3) / 1e12,
                 "decode_gbs": r["bytes"] / (r["ms_decode"] * 1e-3) / 1e9,
@@ -548,6 +607,7 @@ def main():
                 "frac_bf16_peak": r["flops"] / (r["ms_decode"] * 1e-3) / 1e12 / bf16_peak,
                 "frac_hbm_peak": r["bytes"] / (r["ms_decode"] * 1e-3) / 1e9 / hbm_peak,
                 "pieces": r["pieces"], "steps": kx,
+                "roofline": roofline_of(r, name, kernel_of(args.kernel, wx), peaks),
             }
             del gx, cx
             torch.cuda.empty_cache()
@@ -604,8 +664,11 @@ def main():
         "config": {"workload": w.name, "batch": w.b, "s_q": w.s_q, "h_q": w.h_q,
                    "seqlen": int(w.cache_seqlens.max()), "page": 64, "d_qk": 576, "d_v": 512,
                    "causal": w.causal, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV 302 MB vs 129 MB); kernel timing flushes L2"},
+                   "l2": "value: back-to-back step replays, inputs larger than L2 (KV 302 MB "
+                         "vs 129 MB); step_l2_flushed and roofline: L2 flushed before each "
+                         "step / launch"},
         "tflops": tflops, "frac_hbm_peak_step": gbs / world / hbm_peak,
+        "step_l2_flushed": flushed,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 2 * args.steps, "clocks": clocks,
         "kernel_ms": {"sched": res["ms_sched"], "decode": res["ms_decode"],

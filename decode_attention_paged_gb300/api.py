@@ -147,11 +147,20 @@ def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: 
     (see include/mla_decode.h).  The caller passes out and lse; nothing here
     allocates."""
     assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+    assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+    assert meta.dtype == torch.int32 and num_splits.dtype == torch.int32
     b, s_q, h_q, d = q.shape
     assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and q.stride(1) == h_q * D_QK
     num_pages, page, h_kv, dk = k_cache.shape
     assert dk == D_QK and k_cache.stride(3) == 1 and block_table.stride(1) == 1
-    assert out.stride(3) == 1 and lse.is_contiguous() and cache_seqlens.is_contiguous()
+    assert block_table.dim() == 2 and block_table.shape[0] == b
+    assert cache_seqlens.shape == (b,) and cache_seqlens.is_contiguous()
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == (b, s_q, h_q, D_V)
+    assert out.stride(3) == 1
+    assert lse.dtype == torch.float32 and tuple(lse.shape) == (b, h_q, s_q)
+    assert lse.is_contiguous()
+    for t in (k_cache, block_table, cache_seqlens, meta, num_splits, out, lse):
+        assert t.device == q.device, "every tensor must be on q's device"
     with torch.cuda.device(q.device):
         st = _lib.load().mla_decode_fwd_noalloc(
             _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
@@ -324,7 +333,6 @@ def set_fixed_overhead(blocks: int) -> None:
     _lib.check(_lib.load().mla_set_fixed_overhead(int(blocks)), "mla_set_fixed_overhead")
 
 
-KERNEL_PAIR = 0    # one 2-CTA cluster per SM pair, head dims split across the pair
 KERNEL_SINGLE = 1  # one CTA per SM holding all 576 dims
 KERNEL_TQ = 2      # one CTA per SM, most of Q in tensor memory, three KV stages
 KERNEL_AUTO = 3    # default: KERNEL_TQ for s_q * h_q <= 32, else KERNEL_SINGLE

@@ -31,7 +31,6 @@ std::atomic<int> g_kernel{MLA_KERNEL_AUTO};
 struct DeviceInfo {
     std::once_flag once;
     int sms = 0;
-    int pair_clusters = 0;  // co-resident 2-CTA clusters of the pair kernel
     int major = 0, minor = 0;
     int* error_word = nullptr;
     cudaError_t status = cudaSuccess;
@@ -60,10 +59,6 @@ int device_info(DeviceInfo** out) {
             d.status = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (d.status == cudaSuccess)
             d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), g_mla_error_word);
-        if (d.status == cudaSuccess && d.major == 10 && d.minor == 3) {
-            d.pair_clusters = pair_max_active_clusters();
-            if (d.pair_clusters <= 0) d.pair_clusters = d.sms / 2;
-        }
     });
     if (d.status != cudaSuccess) return MLA_ERR_CUDA;
     // The kernels are built for sm_103a only.
@@ -75,12 +70,9 @@ int device_info(DeviceInfo** out) {
 int n_mtiles_of(int R) { return (R + kTileM - 1) / kTileM; }
 
 // SM parts of the split plan: as many (part, query tile) work units as the
-// selected kernel keeps resident at once -- one CTA per SM for the single-CTA
-// kernel, one 2-CTA cluster per SM pair for the pair kernel.
+// decode kernels keep resident at once, one CTA per SM.
 int num_parts_of(int R, const DeviceInfo* d) {
-    const int mt = n_mtiles_of(R);
-    const int units = g_kernel.load() == MLA_KERNEL_PAIR ? d->pair_clusters : d->sms;
-    const int parts = units / mt;
+    const int parts = d->sms / n_mtiles_of(R);
     return parts > 0 ? parts : 1;
 }
 
@@ -106,11 +98,9 @@ int check_shape(int batch, int h_q, int s_q, int h_kv) {
     if (static_cast<int64_t>(s_q) * h_q > (1 << 24)) return MLA_ERR_INVALID_ARGUMENT;
     if (h_kv > 1) {
         // A query tile covers whole head groups of 64 / grp tokens, or a
-        // 64-head slice of one token; only the single-CTA kernel reads several
-        // cache heads.
+        // 64-head slice of one token.
         const int g = h_q / h_kv;
         if (g <= kTileM ? (kTileM % g != 0) : (g % kTileM != 0)) return MLA_ERR_UNSUPPORTED;
-        if (g_kernel.load() == MLA_KERNEL_PAIR) return MLA_ERR_UNSUPPORTED;
     }
     return MLA_OK;
 }
@@ -215,8 +205,7 @@ int mla_set_wait_budget_ns(uint64_t budget_ns) {
 }
 
 int mla_set_decode_kernel(int kind) {
-    if (kind != MLA_KERNEL_PAIR && kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_TQ &&
-        kind != MLA_KERNEL_AUTO)
+    if (kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_TQ && kind != MLA_KERNEL_AUTO)
         return MLA_ERR_INVALID_ARGUMENT;
     g_kernel.store(kind);
     return MLA_OK;
@@ -441,9 +430,8 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     if (kind == MLA_KERNEL_AUTO)  // Q mostly in TMEM wins for tiles of at most 32 rows
         kind = R <= 32 ? MLA_KERNEL_TQ : MLA_KERNEL_SINGLE;
     if (h_kv > 1) kind = MLA_KERNEL_SINGLE;  // the only kernel that reads several cache heads
-    cudaError_t e = kind == MLA_KERNEL_PAIR   ? launch_decode_pair(p, q_map, kv_map, s)
-                    : kind == MLA_KERNEL_TQ   ? launch_decode_tq(p, q_map, kv_map, s)
-                                              : launch_decode(p, q_map, kv_map, s);
+    cudaError_t e = kind == MLA_KERNEL_TQ ? launch_decode_tq(p, q_map, kv_map, s)
+                                          : launch_decode(p, q_map, kv_map, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -644,9 +632,6 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     if (st) return st;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
     if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
-    // The FP8 layout is read by the single-CTA kernel, whose plan the pair
-    // kernel's metadata does not match.
-    if (g_kernel.load() == MLA_KERNEL_PAIR) return MLA_ERR_UNSUPPORTED;
     if (!q_dev || !k_cache_dev || !block_table_dev || !cache_seqlens_dev || !meta_dev ||
         !num_splits_dev || !out_dev || !lse_dev)
         return MLA_ERR_INVALID_ARGUMENT;

@@ -137,9 +137,6 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);
 cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
                              const CUtensorMap& kv_map, cudaStream_t stream);
-cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map,
-                               const CUtensorMap& kv_map, cudaStream_t stream);
-int pair_max_active_clusters();  // on the current device; 0 when the query fails
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 int sched_max_batch();
 

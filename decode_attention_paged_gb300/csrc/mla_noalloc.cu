@@ -23,12 +23,29 @@ constexpr int kMaxNoAllocDevices = 64;
 // Partial outputs and log-sum-exps of split requests, shared by all calls.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Device address of the array, per device.  Only a successful lookup is
+// kept: a lookup that failed (for instance during a stream capture, where the
+// runtime may refuse the call) is tried again on the next call.
 struct ScratchAddress {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t status = cudaSuccess;
+    std::mutex lock;
+    void* ptr = nullptr;  // non-null once resolved
 };
 ScratchAddress g_scratch_address[kMaxNoAllocDevices];
+
+void* scratch_address(int dev) {
+    ScratchAddress& s = g_scratch_address[dev];
+    std::lock_guard<std::mutex> guard(s.lock);
+    if (s.ptr == nullptr) {
+        // The current device is `dev`, so this resolves the array's copy on it.
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) {
+            s.ptr = p;
+        } else {
+            cudaGetLastError();  // clear the error state so that a later call can try again
+        }
+    }
+    return s.ptr;
+}
 
 }  // namespace
 }  // namespace mla
@@ -50,17 +67,13 @@ extern "C" int mla_decode_fwd_noalloc(
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxNoAllocDevices) return MLA_ERR_UNSUPPORTED;
-    ScratchAddress& s = g_scratch_address[dev];
-    std::call_once(s.once, [&] {
-        // The current device is `dev`, so this resolves the array's copy on it.
-        s.status = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch);
-    });
-    if (s.status != cudaSuccess || s.ptr == nullptr) return MLA_ERR_CUDA;
+    void* scratch = scratch_address(dev);
+    if (scratch == nullptr) return MLA_ERR_CUDA;
 
     return mla_decode_fwd(q_dev, q_batch_stride, k_cache_dev, k_page_stride, k_token_stride,
                           num_pages, page_size, block_table_dev, bt_batch_stride,
                           max_blocks_per_seq, cache_seqlens_dev, batch, s_q, h_q, h_kv,
-                          softmax_scale, causal, meta_dev, num_splits_dev, s.ptr,
+                          softmax_scale, causal, meta_dev, num_splits_dev, scratch,
                           kNoAllocScratchBytes, out_dev, out_batch_stride, out_s_stride,
                           out_h_stride, lse_dev, stream);
 }

@@ -160,6 +160,24 @@ def hbm_bytes(seqlens: Sequence[int], s_q: int, h_q: int) -> int:
     return sum(int(L) for L in seqlens) * D_QK * 2 + rows * (D_QK * 2 + D_V * 2 + 4)
 
 
+def unit_work(seqlens: Sequence[int], s_q: int, h_q: int, causal: bool, units) -> tuple:
+    """(bytes, FLOPs) of a sample of (request, row) units, row = s * h_q + h:
+    each row's share of its request's cached tokens (1152 B per token, spread
+    evenly over the request's s_q * h_q rows), its q / out / lse bytes, and
+    2 * (576 + 512) FLOPs per visible key.  Summed over every unit of a
+    workload this is hbm_bytes and flops."""
+    R = s_q * h_q
+    nbytes = 0.0
+    nflops = 0
+    for i, rho in units:
+        L = int(seqlens[int(i)])
+        s = int(rho) // h_q
+        vis = max(0, min(L, L - s_q + s + 1)) if causal else L
+        nbytes += L * D_QK * 2 / R + (D_QK * 2 + D_V * 2 + 4)
+        nflops += vis * 2 * (D_QK + D_V)
+    return nbytes, nflops
+
+
 # ---------------------------------------------------------------- sparse decode
 # Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11): every query token attends
 # to its own list of topk cache positions, index = physical page * 64 + offset.

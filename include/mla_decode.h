@@ -44,8 +44,8 @@
  * j*g .. j*g+g-1 (g = h_q / h_kv) attend to cache head j, each group as in the
  * definition above.  h_q must be a multiple of h_kv, and g must divide 64 or
  * be a multiple of 64 (else MLA_ERR_UNSUPPORTED); the heads of a token are
- * adjacent in the cache (head stride 576).  Not with MLA_KERNEL_PAIR, sparse
- * decode or the FP8 layout (MLA_ERR_UNSUPPORTED).
+ * adjacent in the cache (head stride 576).  Not with sparse decode or the FP8
+ * layout (MLA_ERR_UNSUPPORTED).
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -68,7 +68,7 @@ typedef struct CUstream_st *mla_stream_t; /* same type as cudaStream_t */
 enum {
     MLA_OK = 0,
     MLA_ERR_INVALID_ARGUMENT = -1,   /* null pointer, bad size or stride       */
-    MLA_ERR_UNSUPPORTED = -2,        /* h_kv != 1, page size != 64, wrong GPU   */
+    MLA_ERR_UNSUPPORTED = -2,        /* shape/layout not built, or wrong GPU    */
     MLA_ERR_WORKSPACE_TOO_SMALL = -3,
     MLA_ERR_CUDA = -4,               /* a CUDA runtime call failed              */
     MLA_ERR_DEVICE_TIMEOUT = -5,     /* device: a pipeline wait ran out         */
@@ -273,8 +273,7 @@ MLA_API int mla_decode_fwd_noalloc(const void *q_dev, int64_t q_batch_stride,
  *                apart (>= 41984, a multiple of 16); 16-byte aligned.  A
  *                block-table entry outside [0, num_pages) reads zeros.
  *   everything else as mla_decode_fwd; the metadata from mla_get_metadata.
- * Always runs the single-CTA kernel: returns MLA_ERR_UNSUPPORTED while
- * mla_set_decode_kernel selects MLA_KERNEL_PAIR (whose plan differs).
+ * Always runs the single-CTA kernel (its plan is the same as the TQ kernel's).
  * Enqueues the decode kernel and the combine kernel on `stream`;
  * graph-capturable.
  */
@@ -372,11 +371,6 @@ MLA_API int mla_set_fixed_overhead(int blocks);
  *                     MLA_KERNEL_SINGLE (same split plan for both).
  *   MLA_KERNEL_SINGLE one CTA per SM part and 64-row query tile,
  *                     Q in shared memory, two KV pages in flight.
- *   MLA_KERNEL_PAIR   one 2-CTA cluster per SM pair: the two CTAs split the
- *                     576 head dims, swap their partial QK^T scores through
- *                     distributed shared memory (the cluster exchange of
- *                     "[DeepSeek-3] FlashMLA", sec. 13) and each computes half
- *                     of the 512 output dims.
  *   MLA_KERNEL_TQ     one CTA per SM part and query tile with Q's dims
  *                     0..447 in tensor memory (the A operand of QK^T, as in
  *                     "Blackwell 多轨矩乘(multi-rail GEMM)", sec. 1), so that
@@ -388,7 +382,6 @@ MLA_API int mla_set_fixed_overhead(int blocks);
  * device.  Returns MLA_ERR_INVALID_ARGUMENT for an unknown kind.
  * mla_get_decode_kernel returns the current kind.
  */
-#define MLA_KERNEL_PAIR 0
 #define MLA_KERNEL_SINGLE 1
 #define MLA_KERNEL_TQ 2
 #define MLA_KERNEL_AUTO 3

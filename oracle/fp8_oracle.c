@@ -14,7 +14,7 @@
  * computes dense MLA decode over the dequantised cache
  *     k[c]       = bf16( e4m3(latent[c]) * scale[c / 128] ),  c < 512
  *     k[512 + c] = rope[c]
- * Readings of what the page leaves open (also listed in the design doc):
+ * Readings of what the page leaves open:
  *   - the regions follow each other in the order the page's table lists them;
  *   - dequantisation multiplies the e4m3 value by its scale;
  *   - "to BF16" rounds the exact product to nearest, ties to even;
@@ -23,7 +23,7 @@
  * Here: oracle_fp8_dequant writes the bf16 bit patterns of the dequantised
  * rows; the attention itself is then the dense oracle (mla_oracle.c) on them.
  *
- * Parity status: pinned by tests/test_oracle_fp8.py (e4m3 decoding of all 256
+ * Parity status: pinned by the CPU tests (e4m3 decoding of all 256
  * codes and the bf16 rounding against torch's conversions; the whole
  * dequantisation against a torch-only restatement; power-of-two scales exact).
  */

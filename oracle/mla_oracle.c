@@ -27,9 +27,9 @@
  *   lse is the natural log of the sum of exp(scaled score) ([AttnBook]
  *   "FlashAttention:分块", step 3: m + log l).
  *
- * Parity status: every function here is pinned by tests/test_oracle_pins.py
- * and tests/test_oracle_golden.py (closed forms, library routines, brute
- * force, worked numbers from the pages).  No function is "parity unpinned".
+ * Parity status: every function here is pinned by the CPU tests against
+ * closed forms, library routines, brute force and worked numbers from the
+ * pages.  No function is "parity unpinned".
  */
 #include <math.h>
 #include <pthread.h>

@@ -16,7 +16,7 @@
  *      prefix sum) so the combine step can find them.
  *   The per-part record has the fields of that section's DecodingSchedMeta.
  *
- * Readings of what the page leaves open (each also listed in the design doc):
+ * Readings of what the page leaves open:
  *   - Every request costs its blocks plus one fixed overhead c (c >= 1), so
  *     total = sum_i (n_i + c).  Lay the requests out in order on a line of
  *     cost units: request i owns c overhead units followed by its n_i block

@@ -17,7 +17,7 @@
  *     x_k    = scale * sum_{c<d} q[i][s][h][c] * kv[idx_k][c]
  *     lse[i][h][s] = M + ln sum_k exp(x_k - M),  M = max_k x_k
  *     out[i][s][h] = sum_k exp(x_k - lse) * kv[idx_k][0:dv]
- * Readings of what the page leaves open (also listed in the design doc):
+ * Readings of what the page leaves open:
  *   - an index < 0 is padding: that slot contributes nothing;
  *   - an index >= num_pages * page points outside the cache: it contributes
  *     nothing and the call reports it (return -5);
@@ -26,7 +26,7 @@
  *   - an empty key list gives out = 0 and lse = -inf, as for an empty
  *     sequence in dense decode.
  *
- * Parity status: pinned by tests/test_oracle_sparse.py (equality with the
+ * Parity status: pinned by the CPU tests (equality with the
  * dense oracle when the indices list a request's tokens in order; duplicate
  * keys, padding, the empty list and out-of-range indices in closed form).
  */

@@ -95,23 +95,6 @@ def test_fp8_matches_bf16_decode_of_the_dequantised_cache():
     assert (l8 - lb).abs().max().item() <= 1e-3
 
 
-def test_fp8_rejected_under_the_pair_kernel():
-    from decode_attention_paged_gb300 import api
-
-    w = W.as_fp8(W.random_case(822, 1, 1, 16, [64], False))
-    g = w.to("cuda")
-    default = api.get_decode_kernel()
-    try:
-        api.set_decode_kernel(api.KERNEL_PAIR)
-        meta, ns = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
-        with pytest.raises(_lib.MLAError) as e:
-            api.mla_decode_fp8_fwd(g.q, g.k_cache, g.block_table, g.cache_seqlens,
-                                   w.softmax_scale, False, meta, ns)
-        assert e.value.code == _lib.MLA_ERR_UNSUPPORTED
-    finally:
-        api.set_decode_kernel(default)
-
-
 def test_fp8_memory_bound_full_size_sampled():
     """The memory-bound workload in the FP8 layout at full size, in the launch
     configuration the benchmark times; sampled rows against the oracle."""

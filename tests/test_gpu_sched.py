@@ -50,26 +50,6 @@ def test_device_plan_equals_oracle(seqlens, h_q, s_q):
     check_plan_invariants(seqlens, parts, ns, num_parts, fixed)
 
 
-def test_pair_kernel_uses_one_part_per_cluster():
-    """The 2-CTA cluster kernel: one SM part per co-resident cluster, at most
-    one per SM pair; the plan is still the oracle's for that part count."""
-    from decode_attention_paged_gb300 import api
-
-    default = api.get_decode_kernel()
-    api.set_decode_kernel(api.KERNEL_PAIR)
-    try:
-        for seqlens, h_q, s_q in CASES[:4]:
-            hdr, parts, ns = device_plan(seqlens, h_q, s_q)
-            n_mtiles = int(hdr[4])
-            sms = torch.cuda.get_device_properties(0).multi_processor_count
-            assert 1 <= int(hdr[3]) <= max(1, (sms // 2) // n_mtiles)
-            assert int(hdr[3]) >= max(1, (sms // 2 - 8) // n_mtiles)
-            ref_parts, ref_ns = oracle.plan(seqlens, int(hdr[3]), int(hdr[5]))
-            assert np.array_equal(parts, ref_parts) and np.array_equal(ns, ref_ns)
-    finally:
-        api.set_decode_kernel(default)
-
-
 def test_random_seqlens_plans():
     rng = np.random.default_rng(5)
     for _ in range(20):

@@ -129,3 +129,47 @@ def test_sparse_host_side_argument_checks(lib):
 
     if not torch.cuda.is_available():
         assert call() == E.MLA_ERR_NO_DEVICE
+
+
+def _noalloc_args(**override):
+    """CPU tensors shaped like a valid no-allocation call (b=2, s_q=1, h_q=16)."""
+    import torch
+
+    b, s_q, h_q = 2, 1, 16
+    a = dict(
+        q=torch.zeros(b, s_q, h_q, 576, dtype=torch.bfloat16),
+        k_cache=torch.zeros(4, 64, 1, 576, dtype=torch.bfloat16),
+        block_table=torch.zeros(b, 2, dtype=torch.int32),
+        cache_seqlens=torch.full((b,), 64, dtype=torch.int32),
+        softmax_scale=576 ** -0.5, causal=False,
+        meta=torch.zeros(8 + 8 * 152, dtype=torch.int32),
+        num_splits=torch.zeros(b + 1, dtype=torch.int32),
+        out=torch.zeros(b, s_q, h_q, 512, dtype=torch.bfloat16),
+        lse=torch.zeros(b, h_q, s_q, dtype=torch.float32))
+    a.update(override)
+    return a
+
+
+@pytest.mark.parametrize("bad", [
+    dict(block_table="int64"), dict(cache_seqlens="int64"), dict(out="float32"),
+    dict(out="short"), dict(lse="transposed")])
+def test_noalloc_wrapper_rejects_wrong_dtypes_and_shapes(bad):
+    """The Python wrapper checks what the C ABI cannot see (dtypes and shapes)
+    before it passes raw pointers: an int64 block table would otherwise be read
+    as pairs of int32 words, an undersized out written past its end."""
+    import torch
+
+    from decode_attention_paged_gb300 import api
+
+    a = _noalloc_args()
+    key, kind = next(iter(bad.items()))
+    if kind == "int64":
+        a[key] = a[key].to(torch.int64)
+    elif kind == "float32":
+        a[key] = a[key].float()
+    elif kind == "short":
+        a[key] = a[key][:, :, :, :256]
+    elif kind == "transposed":
+        a[key] = torch.zeros(2, 1, 16, dtype=torch.float32)
+    with pytest.raises(AssertionError):
+        api.mla_decode_fwd_noalloc(**a)

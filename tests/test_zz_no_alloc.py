@@ -7,16 +7,18 @@ workspace.
 
 Checked here, through the C ABI: on two calls in a row (different inputs, so
 the second call runs over scratch the first one left behind) its out / lse
-match those of mla_decode_fwd within the parity tolerances; a problem whose
-scratch would exceed 32 MiB is refused before anything runs.  This file is
+match those of mla_decode_fwd within the parity tolerances, and both match the
+fp64 oracle element by element; a problem whose scratch would exceed 32 MiB is
+refused before anything runs.  This file is
 collected last so a failure here never hides the other tests' results."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from decode_attention_paged_gb300 import _lib
 from decode_attention_paged_gb300 import workloads as W
-from tests._helpers import assert_close
+from tests._helpers import NTHREADS, assert_close, problem
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +39,9 @@ def test_noalloc_matches_fwd_on_two_calls_in_a_row():
         assert api.mla_last_device_error() == 0
         assert int(ns[-1]) > w.b, "the plan should split requests so the scratch is used"
         assert_close(out, lse, ref_out.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
-                     f"noalloc seed {seed}")
+                     f"noalloc seed {seed} against mla_decode_fwd")
+        o_out, o_lse = oracle.mla_decode(problem(w), nthreads=NTHREADS)
+        assert_close(out, lse, o_out, o_lse, f"noalloc seed {seed} against the oracle")
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
