@@ -4,8 +4,7 @@ by element, on seeded inputs.
 - small cases (several 64-row tiles, ragged tails, causal and not, splits):
   every output element;
 - the five benchmark workloads at full size, in the launch configuration the
-  benchmark times: sampled rows recomputed by the oracle, plus properties that
-  hold at any size (all outputs finite);
+  benchmark times: every output element against the oracle;
 - edge cases: empty sequences, one token, causal rows that see nothing,
   NaN-poisoned tails and unreferenced pages, strided tensors, metadata reuse.
 Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3.
@@ -18,8 +17,7 @@ import torch
 
 import oracle
 from decode_attention_paged_gb300 import workloads as W
-from tests._helpers import (NTHREADS, assert_close, gather_units, problem, run_gpu,
-                            sample_units)
+from tests._helpers import NTHREADS, assert_close, problem, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -157,18 +155,11 @@ def test_metadata_reused_across_layers_and_deterministic():
 
 
 @pytest.mark.parametrize("name", ["memory_bound", "compute_bound", "mtp", "long_ragged"])
-def test_benchmark_workloads_full_size_sampled(name):
-    """Full-size workloads in the benchmark's launch configuration; the oracle
-    recomputes a sample of rows one by one."""
+def test_benchmark_workloads_full_size(name):
+    """Full-size workloads in the benchmark's launch configuration: every
+    element of out and lse against the oracle (all rows, all 512 dims)."""
     w = W.CONFIGS[name]()
     out, lse, meta, ns = run_gpu(w)
-    assert torch.isfinite(out).all()
-    L = w.cache_seqlens
-    rows_nonempty = (L > 0).all()
-    if rows_nonempty and not w.causal:
-        assert torch.isfinite(lse).all()
-    units = sample_units(w, 96, seed=sum(map(ord, name)))
-    ref_o, ref_l = oracle.mla_decode_rows(problem(w), units, nthreads=NTHREADS)
-    go, gl = gather_units(out, lse, units, w.h_q)
-    errs = assert_close(torch.from_numpy(go), torch.from_numpy(gl), ref_o, ref_l, name)
+    ref_o, ref_l = oracle.mla_decode(problem(w), nthreads=NTHREADS)
+    errs = assert_close(out, lse, ref_o, ref_l, name)
     print(name, "max errs", errs, "pieces", int(ns[-1].item()))

@@ -103,20 +103,11 @@ def test_sparse_rejects_unpacked_pages():
     assert e.value.code == _lib.MLA_ERR_UNSUPPORTED
 
 
-def test_sparse_workload_full_size_sampled():
+def test_sparse_workload_full_size():
     """The sparse benchmark workload (batch 128, s_q 2, h_q 128, topk 2048) at
-    full size, in the launch configuration the benchmark times; sampled rows
-    against the oracle one by one."""
-    from tests._helpers import gather_units
-
+    full size, in the launch configuration the benchmark times; every element
+    against the oracle."""
     w = W.sparse()
     out, lse = run_gpu_sparse(w)
-    rng = np.random.default_rng(7)
-    R = w.s_q * w.h_q
-    units = {(0, 0), (w.b - 1, R - 1), (w.b // 2, 64), (w.b // 2, 63), (1, w.h_q)}
-    while len(units) < 48:
-        units.add((int(rng.integers(0, w.b)), int(rng.integers(0, R))))
-    units = np.array(sorted(units), dtype=np.int32)
-    ro, rl = oracle.mla_sparse_rows(sparse_problem(w), units, nthreads=NTHREADS)
-    go, gl = gather_units(out, lse, units, w.h_q)
-    assert_close(go, gl, ro, rl, "sparse full size")
+    ro, rl = oracle.mla_sparse(sparse_problem(w), nthreads=NTHREADS)
+    assert_close(out, lse, ro, rl, "sparse full size")
