@@ -66,9 +66,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel", choices=["auto", "single", "tq"], default="auto",
-                    help="decode kernel: auto (default: tq for s_q*h_q <= 32, else single), "
-                         "single CTA, or Q in TMEM")
+    ap.add_argument("--kernel", choices=["auto", "single", "tq", "duo"], default="auto",
+                    help="decode kernel: auto (default: tq for s_q*h_q <= 32, duo for >= 128, "
+                         "else single), single CTA, Q in TMEM, or a CTA pair")
     return ap.parse_args()
 
 
@@ -105,7 +105,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"single": ("decode_kernel", "decode_attention_paged_gb300/csrc/mla_decode.cu"),
-                  "tq": ("decode_tq_kernel", "decode_attention_paged_gb300/csrc/mla_decode_tq.cu")}
+                  "tq": ("decode_tq_kernel", "decode_attention_paged_gb300/csrc/mla_decode_tq.cu"),
+                  "duo": ("decode_duo_kernel", "decode_attention_paged_gb300/csrc/mla_decode_duo.cu")}
 
 
 def kernel_source_hash(kernel="single"):
@@ -207,7 +208,8 @@ def kernel_of(kind, w):
     """Name of the decode kernel a dense call on workload w launches."""
     if kind != "auto":
         return kind
-    return "tq" if w.s_q * w.h_q <= 32 else "single"
+    R = w.s_q * w.h_q
+    return "tq" if R <= 32 else ("duo" if R >= 128 else "single")
 
 
 def roofline_of(res, workload, kname, peaks):
@@ -544,7 +546,7 @@ def main():
     from decode_attention_paged_gb300 import workloads as W_mod
 
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "single": api.KERNEL_SINGLE,
-                           "tq": api.KERNEL_TQ}[args.kernel])
+                           "tq": api.KERNEL_TQ, "duo": api.KERNEL_DUO}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
     # weak scaling: every rank decodes its own batch of requests (replicas).
     w = replica_workload(W_mod, args.workload, rank)

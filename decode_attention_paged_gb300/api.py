@@ -335,7 +335,8 @@ def set_fixed_overhead(blocks: int) -> None:
 
 KERNEL_SINGLE = 1  # one CTA per SM holding all 576 dims
 KERNEL_TQ = 2      # one CTA per SM, most of Q in tensor memory, three KV stages
-KERNEL_AUTO = 3    # default: KERNEL_TQ for s_q * h_q <= 32, else KERNEL_SINGLE
+KERNEL_AUTO = 3    # default: TQ for s_q * h_q <= 32, DUO for >= 128 (one cache head), else SINGLE
+KERNEL_DUO = 4     # a 2-CTA cluster per SM pair, 128-row tiles, pages split by head dims
 
 
 def set_decode_kernel(kind: int) -> None:

@@ -31,6 +31,7 @@ std::atomic<int> g_kernel{MLA_KERNEL_AUTO};
 struct DeviceInfo {
     std::once_flag once;
     int sms = 0;
+    int duo_clusters = 0;  // co-resident 2-CTA clusters of the CTA-pair kernel
     int major = 0, minor = 0;
     int* error_word = nullptr;
     cudaError_t status = cudaSuccess;
@@ -59,6 +60,8 @@ int device_info(DeviceInfo** out) {
             d.status = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (d.status == cudaSuccess)
             d.status = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.error_word), g_mla_error_word);
+        if (d.status == cudaSuccess && d.major == 10 && d.minor == 3)
+            d.duo_clusters = duo_max_active_clusters();
     });
     if (d.status != cudaSuccess) return MLA_ERR_CUDA;
     // The kernels are built for sm_103a only.
@@ -68,11 +71,32 @@ int device_info(DeviceInfo** out) {
 }
 
 int n_mtiles_of(int R) { return (R + kTileM - 1) / kTileM; }
+constexpr int kPairTileM = 128;  // query rows of one CTA pair
+
+// The decode kernel a dense call with R rows per request (h_kv cache heads)
+// launches: the one mla_set_decode_kernel selected, or by tile height.
+int kernel_for(int R, int h_kv, const DeviceInfo* d) {
+    int kind = g_kernel.load();
+    if (kind == MLA_KERNEL_AUTO)
+        kind = R <= 32 ? MLA_KERNEL_TQ : (R >= kPairTileM ? MLA_KERNEL_DUO : MLA_KERNEL_SINGLE);
+    // Several cache heads: the single-CTA kernel only.  The pair kernel loads
+    // 64 query rows per CTA and needs its clusters to be resident.
+    if (h_kv > 1) return MLA_KERNEL_SINGLE;
+    if (kind == MLA_KERNEL_DUO && (R < kTileM || d->duo_clusters < 1)) return MLA_KERNEL_SINGLE;
+    return kind;
+}
+
+// Query tiles of a request for a kernel (64 rows, or 128 for a CTA pair).
+int tiles_of(int R, int kind) {
+    return kind == MLA_KERNEL_DUO ? (R + kPairTileM - 1) / kPairTileM : n_mtiles_of(R);
+}
 
 // SM parts of the split plan: as many (part, query tile) work units as the
-// decode kernels keep resident at once, one CTA per SM.
-int num_parts_of(int R, const DeviceInfo* d) {
-    const int parts = d->sms / n_mtiles_of(R);
+// kernel keeps resident at once -- one CTA per SM, or one cluster per SM pair.
+int num_parts_of(int R, int h_kv, const DeviceInfo* d) {
+    const int kind = kernel_for(R, h_kv, d);
+    const int units = kind == MLA_KERNEL_DUO ? d->duo_clusters : d->sms;
+    const int parts = units / tiles_of(R, kind);
     return parts > 0 ? parts : 1;
 }
 
@@ -205,7 +229,8 @@ int mla_set_wait_budget_ns(uint64_t budget_ns) {
 }
 
 int mla_set_decode_kernel(int kind) {
-    if (kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_TQ && kind != MLA_KERNEL_AUTO)
+    if (kind != MLA_KERNEL_SINGLE && kind != MLA_KERNEL_TQ && kind != MLA_KERNEL_AUTO &&
+        kind != MLA_KERNEL_DUO)
         return MLA_ERR_INVALID_ARGUMENT;
     g_kernel.store(kind);
     return MLA_OK;
@@ -225,7 +250,7 @@ int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
-    const int parts = num_parts_of(g.R, d);
+    const int parts = num_parts_of(g.R, h_kv, d);
     if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
     if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(g.nreq) + 1);
     return MLA_OK;
@@ -242,9 +267,9 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
-    const int parts = num_parts_of(g.R, d);
+    const int parts = num_parts_of(g.R, h_kv, d);
     cudaError_t e = launch_sched(cache_seqlens_dev, h_kv, -1, g.nreq, g.R, parts,
-                                 n_mtiles_of(g.R), g_fixed_overhead.load(),
+                                 tiles_of(g.R, kernel_for(g.R, h_kv, d)), g_fixed_overhead.load(),
                                  static_cast<int32_t*>(meta_dev), num_splits_dev,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -258,7 +283,7 @@ int mla_workspace_size(int batch, int h_q, int s_q, int h_kv, size_t* bytes) {
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     size_t ob = 0;
-    workspace_layout(g.nreq, g.R, num_parts_of(g.R, d), &ob, bytes);
+    workspace_layout(g.nreq, g.R, num_parts_of(g.R, h_kv, d), &ob, bytes);
     return MLA_OK;
 }
 
@@ -288,7 +313,7 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, g.nreq, g.R,
-                        num_parts_of(g.R, d), s_q, h_q, 0, g.kvh, g.grp, out_dev,
+                        num_parts_of(g.R, h_kv, d), s_q, h_q, 0, g.kvh, g.grp, out_dev,
                         out_batch_stride, out_s_stride, out_h_stride, lse_dev, stream);
 }
 
@@ -354,7 +379,8 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     const int R = g.R;
-    const int parts = num_parts_of(R, d);
+    const int parts = num_parts_of(R, h_kv, d);
+    const int kind = kernel_for(R, h_kv, d);
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(g.nreq, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -362,6 +388,7 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
 
     CUtensorMap q_map, kv_map;
     uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
+    if (kind == MLA_KERNEL_DUO) q_box_rows = kTileM;  // each CTA of a pair loads 64 rows
     if (h_kv == 1) {
         st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
                        kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
@@ -414,7 +441,7 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.s_q = s_q;
     p.h_q = h_q;
     p.R = R;
-    p.n_mtiles = n_mtiles_of(R);
+    p.n_mtiles = tiles_of(R, kind);
     p.num_parts = parts;
     p.q_box_rows = static_cast<int>(q_box_rows);
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -426,12 +453,9 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.grp = g.grp;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int kind = g_kernel.load();
-    if (kind == MLA_KERNEL_AUTO)  // Q mostly in TMEM wins for tiles of at most 32 rows
-        kind = R <= 32 ? MLA_KERNEL_TQ : MLA_KERNEL_SINGLE;
-    if (h_kv > 1) kind = MLA_KERNEL_SINGLE;  // the only kernel that reads several cache heads
-    cudaError_t e = kind == MLA_KERNEL_TQ ? launch_decode_tq(p, q_map, kv_map, s)
-                                          : launch_decode(p, q_map, kv_map, s);
+    cudaError_t e = kind == MLA_KERNEL_TQ    ? launch_decode_tq(p, q_map, kv_map, s)
+                    : kind == MLA_KERNEL_DUO ? launch_decode_duo(p, q_map, kv_map, s)
+                                             : launch_decode(p, q_map, kv_map, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -649,7 +673,9 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const int R = s_q * h_q;
-    const int parts = num_parts_single(R, d);
+    // The plan is mla_get_metadata's (whatever kernel it was sized for); the
+    // single-CTA kernel runs it with its own 64-row tiles.
+    const int parts = num_parts_of(R, 1, d);
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(batch, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;

@@ -344,8 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = (smem_u32(smem) & 1023u) == 0;
     const int32_t* hdr = p.meta;
     if (ok && (hdr[kHMagic] != kMetaMagic || hdr[kHBatch] != p.batch || hdr[kHRows] != p.R ||
-               hdr[kHParts] != p.num_parts || hdr[kHMTiles] != p.n_mtiles ||
-               hdr[kHPage] != kPage))
+               hdr[kHParts] != p.num_parts || hdr[kHPage] != kPage))
         ok = false;
     Part part{};
     if (ok) {

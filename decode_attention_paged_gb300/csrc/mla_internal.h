@@ -57,7 +57,7 @@ struct DecodeParams {
     float* oaccum;    // [pieces][R][512]
     float* lseaccum;  // [pieces][R], log2 domain
     int batch, s_q, h_q, R, n_mtiles, num_parts;
-    int q_box_rows;   // rows one Q tile load brings (min(64, R))
+    int q_box_rows;   // rows one Q tile load brings (min(64, R); 64 in the CTA-pair kernel)
     float scale_log2; // softmax_scale * log2(e)
     int causal;
     int* error_word;
@@ -137,6 +137,9 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream);
 cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
                              const CUtensorMap& kv_map, cudaStream_t stream);
+cudaError_t launch_decode_duo(const DecodeParams& p, const CUtensorMap& q_map,
+                              const CUtensorMap& kv_map, cudaStream_t stream);
+int duo_max_active_clusters();  // on the current device; 0 when the query fails
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 int sched_max_batch();
 

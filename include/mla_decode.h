@@ -367,8 +367,9 @@ MLA_API int mla_set_fixed_overhead(int blocks);
 /*
  * mla_set_decode_kernel -- which decode kernel mla_decode_fwd and
  * mla_decode_splitkv launch.  Process-wide; all compute the same function.
- *   MLA_KERNEL_AUTO   (default) MLA_KERNEL_TQ when s_q * h_q <= 32, else
- *                     MLA_KERNEL_SINGLE (same split plan for both).
+ *   MLA_KERNEL_AUTO   (default) MLA_KERNEL_TQ when s_q * h_q <= 32,
+ *                     MLA_KERNEL_DUO when s_q * h_q >= 128 (one cache head),
+ *                     else MLA_KERNEL_SINGLE.
  *   MLA_KERNEL_SINGLE one CTA per SM part and 64-row query tile,
  *                     Q in shared memory, two KV pages in flight.
  *   MLA_KERNEL_TQ     one CTA per SM part and query tile with Q's dims
@@ -376,6 +377,14 @@ MLA_API int mla_set_fixed_overhead(int blocks);
  *                     "Blackwell 多轨矩乘(multi-rail GEMM)", sec. 1), so that
  *                     three KV pages fit in shared memory for tiles of at
  *                     most 32 query rows (two otherwise).
+ *   MLA_KERNEL_DUO    a 2-CTA cluster per SM pair and 128-row query tile:
+ *                     the two CTAs split every page by head dims, and one
+ *                     tcgen05 MMA (cta_group::2, M = 128) feeds all 128 rows
+ *                     from each K/V byte; Q's two halves of the latent dims
+ *                     sit in the two TMEM lane groups and the partial QK^T
+ *                     scores are added after the MMA ("Blackwell 多轨矩乘
+ *                     (multi-rail GEMM)", sec. 2 and 4.3).  Tiles of 128 rows
+ *                     and one cache head (otherwise MLA_KERNEL_SINGLE runs).
  * The split plan depends on the kernel (its number of SM parts), so metadata
  * must be rebuilt after a switch; a decode call with metadata built for a
  * kernel with another part count records MLA_ERR_METADATA_MISMATCH on the
@@ -385,6 +394,7 @@ MLA_API int mla_set_fixed_overhead(int blocks);
 #define MLA_KERNEL_SINGLE 1
 #define MLA_KERNEL_TQ 2
 #define MLA_KERNEL_AUTO 3
+#define MLA_KERNEL_DUO 4
 MLA_API int mla_set_decode_kernel(int kind);
 MLA_API int mla_get_decode_kernel(void);
 

@@ -104,8 +104,8 @@ def _timeout_then_recover(run, check):
     check(out, lse)
 
 
-@pytest.mark.parametrize("kind,h_q", [(2, 16), (1, 64), (1, 128)],
-                         ids=["tq", "single-stageP", "single-Pbuffer"])
+@pytest.mark.parametrize("kind,h_q", [(2, 16), (1, 64), (1, 128), (4, 128), (4, 256)],
+                         ids=["tq", "single-stageP", "single-Pbuffer", "duo", "duo-2tiles"])
 def test_every_dense_kernel_unwinds_on_timeout(kind, h_q):
     from decode_attention_paged_gb300 import api
 

@@ -1,6 +1,6 @@
-"""Every dense decode kernel (the single-CTA one, and the one that keeps most of
-the query tile in tensor memory) against the fp64 oracle on the same seeded
-cases, and the two against each other.
+"""Every dense decode kernel (the single-CTA one, the one that keeps most of the
+query tile in tensor memory, and the CTA-pair one for 128-row tiles) against
+the fp64 oracle on the same seeded cases, and against each other.
 Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3."""
 import numpy as np
 import pytest
@@ -25,6 +25,12 @@ CASES = [
     (8, 1, 16, [4096] * 8, False),
     (128, 1, 16, [512] * 128, False),
     (24, 2, 16, [700] * 24, True),
+    # 128-row tiles (the CTA-pair kernel's shape): one and two tiles per
+    # request, a partial second tile, splits, empty requests, causal MTP
+    (3, 1, 128, [0, 5000, 77], False),
+    (4, 2, 128, [64, 1, 4097, 300], True),
+    (2, 1, 200, [64, 6500], False),
+    (40, 1, 128, [1000] * 40, False),
 ]
 
 
@@ -38,7 +44,7 @@ def kernel_kind(request):
     api.set_decode_kernel(default)
 
 
-@pytest.mark.parametrize("kernel_kind", [1, 2], indirect=True, ids=["single", "tq"])
+@pytest.mark.parametrize("kernel_kind", [1, 2, 4], indirect=True, ids=["single", "tq", "duo"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
 def test_kernel_parity(kernel_kind, case):
     b, s_q, h_q, seqlens, causal = case
@@ -68,6 +74,17 @@ def test_kernels_agree():
         # same function, same plan, different summation orders
         assert (o_r.float() - o_one.float()).abs().max().item() <= 2e-2
         assert (l_r - l_one).abs().max().item() <= 1e-3
+        w2 = W.random_case(334, 3, 2, 128, [5000, 70, 900], True)
+        g2 = w2.to("cuda")
+        outs = []
+        for kind in (api.KERNEL_SINGLE, api.KERNEL_DUO):
+            api.set_decode_kernel(kind)
+            m2, n2 = api.mla_get_metadata(g2.cache_seqlens, w2.h_q, w2.s_q)
+            outs.append(api.mla_decode_fwd(g2.q, g2.k_cache, g2.block_table, g2.cache_seqlens,
+                                           w2.softmax_scale, w2.causal, m2, n2))
+            assert api.mla_last_device_error() == 0
+        assert (outs[0][0].float() - outs[1][0].float()).abs().max().item() <= 2e-2
+        assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-3
     finally:
         api.set_decode_kernel(default)
     assert api.get_decode_kernel() == default

@@ -39,10 +39,17 @@ def test_device_plan_equals_oracle(seqlens, h_q, s_q):
     R = s_q * h_q
     assert hdr[0] == 0x4D4C4131 and hdr[1] == len(seqlens) and hdr[2] == R
     num_parts, n_mtiles, fixed = int(hdr[3]), int(hdr[4]), int(hdr[5])
-    assert n_mtiles == -(-R // 64)
-    # the default kernel runs one CTA per SM: one SM part per SM and tile
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert num_parts == max(1, sms // n_mtiles)
+    if R >= 128:
+        # the default for 128-row tiles is the CTA-pair kernel: one part per
+        # co-resident 2-CTA cluster and 128-row tile, at most one per SM pair
+        assert n_mtiles == -(-R // 128)
+        assert 1 <= num_parts <= max(1, (sms // 2) // n_mtiles)
+        assert num_parts >= max(1, (sms // 2 - 8) // n_mtiles)
+    else:
+        # one CTA per SM: one SM part per SM and 64-row tile
+        assert n_mtiles == -(-R // 64)
+        assert num_parts == max(1, sms // n_mtiles)
     ref_parts, ref_ns = oracle.plan(seqlens, num_parts, fixed)
     assert np.array_equal(parts, ref_parts)
     assert np.array_equal(ns, ref_ns)
