@@ -46,8 +46,8 @@
 // five 40 KB stages, preceded by two pseudo-pages per request that carry its
 // 64 query rows (chunks 0, 1, 4, 5, 8 and 2, 3, 6, 7).  The peer's otherwise
 // idle MMA warp forwards "my half has landed" to the leader (a remote
-// mbarrier arrive); the leader's MMA warp issues QK^T and PV for both CTAs and
-// commits to barriers in both.  Eight softmax warps per CTA (two per SM
+// mbarrier arrive); the leader's QK^T and PV warps issue the MMAs for both
+// CTAs and commit to barriers in both.  Eight softmax warps per CTA (two per SM
 // sub-partition) each take 16 tokens of a row: warp w reads TMEM lane quadrant
 // w % 4 (rows and rail) and token half w / 4.  P goes into slot 4 of the
 // page's stage, which QK^T is done with (the peer's producer zeroes it again
@@ -64,6 +64,7 @@ namespace {
 
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kPvWarp = 10;      // the leader's PV issuer
 constexpr int kRelayWarp0 = 10;  // warps 10, 11: the peer's relays
 constexpr int kThreads = 384;
 constexpr int kPairRows = 128;  // query rows of one CTA pair
@@ -113,7 +114,7 @@ struct Barriers {
     uint64_t pv_done[2];         // PV of a page finished (both CTAs)
     uint64_t q_ready;            // leader: both CTAs copied a request's Q
     uint64_t o_free;             // leader: all 16 softmax warps read O in the epilogue
-    uint64_t drain;              // leader: every MMA finished
+    uint64_t drain;              // leader: every MMA of both issuers finished
     uint64_t q_copied;           // peer: its softmax warps copied a request's Q (entries landed)
     uint64_t s_relay[2];         // peer: its 8 softmax warps read S (relayed to s_empty)
     uint64_t p_relay[2];         // peer: its 8 softmax warps wrote P (relayed to p_full)
@@ -186,15 +187,47 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     __syncwarp();
     return ok;
 }
+// Warp-uniform bounded wait of the leader's issuer warps on barriers whose
+// phases complete by remote arrivals from the peer: a thread suspended in
+// mbarrier.try_wait was measured to notice such a phase about a microsecond
+// late, so these poll with the non-suspending test_wait and a short sleep.
+__device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) {
+        if (!mbar_test_wait_cluster(bar, parity)) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t spin = 1;; ++spin) {
+                __nanosleep(32);
+                if (mbar_test_wait_cluster(bar, parity)) break;
+                if ((spin & 63) == 0) {
+                    if (*wc.abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > wc.budget_ns) {
+                        raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
 // One arrival per warp on a barrier of the leader CTA (a remote arrival from
-// the peer), releasing every lane's earlier writes at cluster scope.
+// the peer).  Relaxed: what the leader acts on is already complete (TMEM
+// reads and stores waited for, shared-memory operands fenced for the tensor
+// core by their writers).
 __device__ __forceinline__ void warp_arrive_leader(uint64_t* bar, bool leader) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
         if (leader)
             mbar_arrive(bar);
         else
-            mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
+            mbar_arrive_remote_relaxed(mapa_shared(smem_u32(bar), 0));
     }
 }
 
@@ -245,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&bars->q_ready, 2);
         mbar_init(&bars->o_free, 16);
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain, 2);  // the QK^T and PV issuers
         mbar_init(&bars->q_copied, 1);
         fence_barrier_init();
         prefetch_tensormap(&q_map);
@@ -393,116 +426,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t n = c.ring();
             if (c.blk == c.b0 && !warp_wait(&bars->q_copied, c.item & 1, wc)) break;
             if (!warp_wait(&bars->kv_full[n % kStages], (n / kStages) & 1, wc)) break;
-            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&bars->kv_peer[n % kStages]), 0));
+            if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&bars->kv_peer[n % kStages]), 0));
             __syncwarp();
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------ leader: MMA issuer
+        // ----------------------------------------------- leader: QK^T issuer
         // QK^T of page g needs both halves of its page, the request's Q in
-        // both CTAs and a free S buffer; PV of page g needs P(g) from all
-        // sixteen softmax warps (and, on a request's first page, O released by
-        // the previous epilogue).  Lane 0 probes the barriers without blocking
-        // and broadcasts; one elected thread issues each burst and its commits.
+        // both CTAs and a free S buffer (both CTAs' softmax warps read S of
+        // page g - 2).  One wait after another (a loop probing several
+        // barriers in turn answered late); the barriers the peer completes are
+        // polled (warp_poll).  One elected thread issues the burst and its
+        // commit.
         constexpr uint32_t idesc_qk = idesc_bf16_f32(kPairRows, 128, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kPairRows, 256, false, true);
         constexpr uint64_t kStageUnits = kStageBytes >> 4, kSlotUnits = kSlotBytes >> 4;
         const uint64_t dK0 = smem_desc(smem_u32(ring), 16, 1024);
-        const uint64_t dV0 = smem_desc(smem_u32(ring), kSlotBytes, 1024);
-        const uint64_t dP0 = smem_desc(smem_u32(ring + 4 * kSlotBytes), 16, 1024);
         const uint64_t dQr = smem_desc(smem_u32(sQr), 16, 1024);
-        const uint32_t tO = tmem + kColO, tQ = tmem + kColQ, tS = tmem + kColS;
-        Cursor qk = cursor_begin(p, part), pv = qk;
+        const uint32_t tQ = tmem + kColQ, tS = tmem + kColS;
         uint32_t peer_par = 0;  // bit s: parity of the next kv_peer[s] phase
-        uint64_t idle_since = 0;
-        uint32_t idle_spins = 0;
-        while (pv.valid) {
-            bool did = false;
-            if (pv.g < qk.g) {
-                const bool first = pv.blk == pv.b0;
-                bool ready = false;
-                if (lane == 0) {
-                    ready = mbar_test_wait_cluster(&bars->p_full[pv.g & 1], (pv.g >> 1) & 1);
-                    if (ready && first && pv.item > 0)
-                        ready = mbar_test_wait_cluster(&bars->o_free, (pv.item - 1) & 1);
-                }
-                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-                if (ready) {
-                    tc_fence_after();
-                    const uint32_t st = pv.ring() % kStages;
-                    const uint64_t aP = dP0 + st * kStageUnits, bV = dV0 + st * kStageUnits;
-                    if (elect_one()) {
+        for (Cursor qk = cursor_begin(p, part); qk.valid; cursor_next(p, part, qk)) {
+            const uint32_t n = qk.ring(), st = n % kStages;
+            // (q_ready first: it also covers the landing of the request's
+            // query entries, which share stages with its pages.)
+            if (qk.blk == qk.b0 && !warp_poll(&bars->q_ready, qk.item & 1, wc)) break;
+            if (!warp_wait(&bars->kv_full[st], (n / kStages) & 1, wc)) break;
+            if (!warp_poll(&bars->kv_peer[st], (peer_par >> st) & 1, wc)) break;
+            if (qk.g >= 2 && !warp_poll(&bars->s_empty[qk.g & 1], ((qk.g >> 1) + 1) & 1, wc)) break;
+            tc_fence_after();
+            const uint64_t bK = dK0 + st * kStageUnits;
+            const uint32_t d = tS + 64 * (qk.g & 1);
+            if (elect_one()) {
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh)
+                for (int j = 0; j < 16; ++j)
+                    mma_pair_ts(d, tQ + 8 * j, bK + (j >> 2) * kSlotUnits + 2 * (j & 3), idesc_qk,
+                                j ? 1u : 0u);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_pair_ss(tO + 128 * hh, aP + 2 * kk,
-                                            bV + 2 * hh * kSlotUnits + 128 * kk, idesc_pv,
-                                            (first && kk == 0) ? 0u : 1u);
-                        mma_commit_pair(&bars->pv_done[pv.g & 1], kBothCtas);
-                        mma_commit_pair(&bars->kv_empty[st], kBothCtas);
-                    }
-                    __syncwarp();
-                    cursor_next(p, part, pv);
-                    did = true;
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_pair_ss(d, dQr + 2 * kk, bK + 4 * kSlotUnits + 2 * kk, idesc_qk, 1u);
+                mma_commit_pair(&bars->s_full[qk.g & 1], kBothCtas);
             }
-            if (qk.valid) {
-                const uint32_t n = qk.ring(), st = n % kStages;
-                bool ready = true;
-                if (lane == 0) {
-                    if (qk.blk == qk.b0) ready = mbar_test_wait_cluster(&bars->q_ready, qk.item & 1);
-                    ready = ready && mbar_test_wait(&bars->kv_full[st], (n / kStages) & 1);
-                    ready = ready && mbar_test_wait_cluster(&bars->kv_peer[st], (peer_par >> st) & 1);
-                    if (ready && qk.g >= 2)
-                        ready = mbar_test_wait_cluster(&bars->s_empty[qk.g & 1],
-                                                       ((qk.g >> 1) + 1) & 1);
-                }
-                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-                if (ready) {
-                    tc_fence_after();
-                    const uint64_t bK = dK0 + st * kStageUnits;
-                    const uint32_t d = tS + 64 * (qk.g & 1);
-                    if (elect_one()) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            mma_pair_ts(d, tQ + 8 * j, bK + (j >> 2) * kSlotUnits + 2 * (j & 3),
-                                        idesc_qk, j ? 1u : 0u);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_pair_ss(d, dQr + 2 * kk, bK + 4 * kSlotUnits + 2 * kk, idesc_qk, 1u);
-                        mma_commit_pair(&bars->s_full[qk.g & 1], kBothCtas);
-                    }
-                    __syncwarp();
-                    peer_par ^= 1u << st;
-                    cursor_next(p, part, qk);
-                    did = true;
-                }
-            }
-            if (did) {
-                idle_since = 0;
-                idle_spins = 0;
-                continue;
-            }
-            __nanosleep(32);
-            if ((++idle_spins & 63) == 0) {
-                bool stop = false;
-                if (lane == 0) {
-                    if (*abort_flag) {
-                        stop = true;
-                    } else {
-                        const uint64_t now = globaltimer_ns();
-                        if (idle_since == 0) {
-                            idle_since = now;
-                        } else if (now - idle_since > p.budget_ns) {
-                            raise_error(wc, MLA_ERR_DEVICE_TIMEOUT);
-                            stop = true;
-                        }
-                    }
-                }
-                if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) break;
-            }
+            __syncwarp();
+            peer_par ^= 1u << st;
         }
         // Drain: every MMA finished before the CTAs meet at the final barrier.
+        if (elect_one()) mma_commit_pair(&bars->drain, kLeaderCta);
+        __syncwarp();
+        if (lane == 0) mbar_drain(&bars->drain, 0, kDrainBudgetNs);
+        __syncwarp();
+    } else if (leader && warp == kPvWarp) {
+        // ------------------------------------------------- leader: PV issuer
+        // PV of page g needs P(g) from both CTAs' softmax warps (and, on a
+        // request's first page, O released by the previous epilogue).  Its
+        // commits free the page's stage in both CTAs (PV(g) finishes after
+        // QK^T(g), issued earlier into the same tensor pipe).
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kPairRows, 256, false, true);
+        constexpr uint64_t kStageUnits = kStageBytes >> 4, kSlotUnits = kSlotBytes >> 4;
+        const uint64_t dV0 = smem_desc(smem_u32(ring), kSlotBytes, 1024);
+        const uint64_t dP0 = smem_desc(smem_u32(ring + 4 * kSlotBytes), 16, 1024);
+        const uint32_t tO = tmem + kColO;
+        for (Cursor pv = cursor_begin(p, part); pv.valid; cursor_next(p, part, pv)) {
+            const bool first = pv.blk == pv.b0;
+            if (!warp_poll(&bars->p_full[pv.g & 1], (pv.g >> 1) & 1, wc)) break;
+            if (first && pv.item > 0 && !warp_poll(&bars->o_free, (pv.item - 1) & 1, wc)) break;
+            tc_fence_after();
+            const uint32_t st = pv.ring() % kStages;
+            const uint64_t aP = dP0 + st * kStageUnits, bV = dV0 + st * kStageUnits;
+            if (elect_one()) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_pair_ss(tO + 128 * hh, aP + 2 * kk, bV + 2 * hh * kSlotUnits + 128 * kk,
+                                    idesc_pv, (first && kk == 0) ? 0u : 1u);
+                mma_commit_pair(&bars->pv_done[pv.g & 1], kBothCtas);
+                mma_commit_pair(&bars->kv_empty[st], kBothCtas);
+            }
+            __syncwarp();
+        }
         if (elect_one()) mma_commit_pair(&bars->drain, kLeaderCta);
         __syncwarp();
         if (lane == 0) mbar_drain(&bars->drain, 0, kDrainBudgetNs);
@@ -583,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) {
                     mbar_arrive(&bars->q_ready);
                 } else {
-                    mbar_arrive_remote(mapa_shared(smem_u32(&bars->q_ready), 0));
+                    mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&bars->q_ready), 0));
                     mbar_arrive(&bars->q_copied);
                 }
             }
@@ -837,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* target = warp == kRelayWarp0 ? bars->s_empty : bars->p_full;
         for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
             if (!warp_wait(&relay[c.g & 1], (c.g >> 1) & 1, wc)) break;
-            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&target[c.g & 1]), 0));
+            if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&target[c.g & 1]), 0));
             __syncwarp();
         }
     }

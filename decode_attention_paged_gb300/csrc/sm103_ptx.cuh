@@ -462,6 +462,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster without release
+// semantics (half the latency of the releasing form when measured in
+// isolation on sm_103a): for signals whose data needs no publication -- TMEM
+// reads or stores already completed, or shared-memory writes already fenced
+// for the tensor core (fence.proxy.async) by the threads that made them.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
 // try_wait with cluster-scope acquire: for phases completed by peer CTAs.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
