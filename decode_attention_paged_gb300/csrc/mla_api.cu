@@ -341,6 +341,7 @@ int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* work
     c.s_q = s_q;
     c.h_q = h_q;
     c.R = R;
+    c.num_parts = parts;
     c.fold = fold;
     c.kvh = kvh;
     c.grp = grp;

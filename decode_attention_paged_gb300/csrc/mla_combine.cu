@@ -8,20 +8,20 @@
 // cudaGridDependencySynchronize (griddepcontrol.wait) and reads the partials
 // with ordinary loads (not the read-only path, which does not see the
 // producer's writes under programmatic launch).  Pieces whose lse is -inf
-// (nothing visible) get weight 0 (their partial rows are written as zeros); if every piece is empty the row is 0 and
-// lse -inf ("CUTLASS 从零重写 FlashAttention：Split KV 并行优化实战", sec. 3.3).
+// (nothing visible) get weight 0 (their partial rows are written as zeros);
+// if every piece is empty the row is 0 and lse -inf ("CUTLASS 从零重写
+// FlashAttention：Split KV 并行优化实战", sec. 3.3).
 //
 // Layout: oaccum [pieces][R][512] fp32 holds each piece's normalised output,
 // lseaccum [pieces][R] its log2-domain log-sum-exp (m + log2 l, with scores
-// already multiplied by softmax_scale * log2 e).  A warp owns one row: lane l
-// owns dims [16 l, 16 l + 16), so each piece is read as one contiguous 2 KB
-// burst per warp with 16-byte vector loads.
+// already multiplied by softmax_scale * log2 e).  A warp works on one row:
+// lane l owns dims [16 l, 16 l + 16), so each piece is read as one contiguous
+// 2 KB burst per warp with 16-byte vector loads.  Rows cut into many pieces get
+// several warps each, which split the pieces and add their partial sums.
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace mla {
-
-constexpr int kCombineWarps = 4;
 
 __device__ __forceinline__ float4 ld_f4(const float* p) {
     // Plain (coherent) global load; see the note on programmatic launch above.
@@ -42,85 +42,125 @@ __device__ __forceinline__ int ld_i(const int32_t* p) {
     return v;
 }
 
-__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombineParams p) {
+// kW warps per query row (kWarps / kW rows per CTA): warp j of a row takes
+// the pieces k = j, j + kW, ..., so a row cut into many pieces streams them
+// from several warps at once; the kW partial sums meet in shared memory.
+template <int kW, int kWarps>
+__global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineParams p) {
+    constexpr int kCombineWarps = kWarps;
+    constexpr int kRowsPerCta = kCombineWarps / kW;
+    __shared__ float4 s_acc[kW > 1 ? kCombineWarps : 1][32][4];
+    __shared__ float s_w[kW > 1 ? kCombineWarps : 1];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int req = blockIdx.y;
-    const int row = blockIdx.x * kCombineWarps + warp;
+    const int row = blockIdx.x * kRowsPerCta + warp / kW;
+    const int j = warp % kW;
     // The next decode grid may launch now: it waits for this grid's completion
     // before it reads its plan or writes anything.
     pdl_launch_dependents();
     pdl_wait_primary();
-    if (row >= p.R) return;
     // Metadata built for another shape: the decode kernel has already recorded
-    // MLA_ERR_METADATA_MISMATCH; num_splits may be too short to index.
+    // MLA_ERR_METADATA_MISMATCH; num_splits may be too short to index.  (Every
+    // condition below is the same for all warps of a CTA, or for all warps of
+    // a row: no warp leaves while its row's partners still need the barrier.)
     if (ld_i(p.meta + kHMagic) != kMetaMagic || ld_i(p.meta + kHBatch) != p.batch ||
         ld_i(p.meta + kHRows) != p.R)
         return;
     const int first = ld_i(p.num_splits + req);
     const int n = ld_i(p.num_splits + req + 1) - first;
     if (n <= 1) return;  // the decode kernel wrote this request directly
+    const bool row_ok = row < p.R;
 
+    // The largest piece lse of the row (every warp of the row computes it).
     const float* lse_base = p.lseaccum + static_cast<int64_t>(first) * p.R + row;
     float mx = -INFINITY;
-    for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ld_f(lse_base + static_cast<int64_t>(k) * p.R));
+    if (row_ok)
+        for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ld_f(lse_base + static_cast<int64_t>(k) * p.R));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
 
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    if (row_ok && mx != -INFINITY) {
+        const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
+        const int64_t piece_stride = static_cast<int64_t>(p.R) * kDv;
+        // Pieces j, j + kW, ...: lane t of each group of 32 holds piece
+        // j + kW (base + t)'s weight; the partial rows are streamed with four
+        // pieces' loads in flight.  An empty piece (lse = -inf) has weight 0
+        // and an all-zero partial row.
+        const int mine = n > j ? (n - j + kW - 1) / kW : 0;  // pieces of this warp
+        for (int base = 0; base < mine; base += 32) {
+            const int t = base + lane;
+            const float lk = t < mine ? ld_f(lse_base + static_cast<int64_t>(j + kW * t) * p.R) : -INFINITY;
+            const float wl = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
+            float ws = wl;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+            wsum += ws;
+            const int m = min(32, mine - base);
+            for (int j0 = 0; j0 < m; j0 += 4) {
+                float4 x[4][4];
+                float w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    w[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
+                    if (j0 + u < m) {
+                        const float* src =
+                            o_base + static_cast<int64_t>(j + kW * (base + j0 + u)) * piece_stride;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) x[u][v] = ld_f4(src + 4 * v);
+                    } else {
+                        w[u] = 0.f;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        acc[4 * v + 0] += w[u] * x[u][v].x;
+                        acc[4 * v + 1] += w[u] * x[u][v].y;
+                        acc[4 * v + 2] += w[u] * x[u][v].z;
+                        acc[4 * v + 3] += w[u] * x[u][v].w;
+                    }
+            }
+        }
+    }
+    if (kW > 1) {
+        // The row's kW partial sums meet in shared memory; its first warp adds
+        // them in a fixed order.
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            s_acc[warp][lane][v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+        if (lane == 0) s_w[warp] = wsum;
+        __syncthreads();
+        if (j != 0) return;
+        for (int q = 1; q < kW; ++q) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 o = s_acc[warp + q][lane][v];
+                acc[4 * v] += o.x;
+                acc[4 * v + 1] += o.y;
+                acc[4 * v + 2] += o.z;
+                acc[4 * v + 3] += o.w;
+            }
+            wsum += s_w[warp + q];
+        }
+    }
+    if (!row_ok) return;
     const OutMap om =
         out_map(req, row, p.h_q, p.s_q, p.fold, p.kvh, p.grp, p.out_sb, p.out_ss, p.out_sh);
     __nv_bfloat16* orow = p.out + om.out_off + lane * 16;
     float* lse_out = p.lse + om.lse_idx;
     if (mx == -INFINITY) {
-        uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 z = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4*>(orow)[0] = z;
         reinterpret_cast<uint4*>(orow)[1] = z;
         if (lane == 0) *lse_out = -INFINITY;
         return;
-    }
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    float wsum = 0.f;
-    const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
-    const int64_t piece_stride = static_cast<int64_t>(p.R) * kDv;
-    // Lane k of each group of 32 pieces holds piece k's weight; the partial
-    // rows are then streamed with all loads of a group of four in flight.
-    // An empty piece (lse = -inf) has weight 0 and an all-zero partial row.
-    for (int base = 0; base < n; base += 32) {
-        const int k = base + lane;
-        const float lk = k < n ? ld_f(lse_base + static_cast<int64_t>(k) * p.R) : -INFINITY;
-        const float wl = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
-        float ws = wl;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-        wsum += ws;
-        const int m = min(32, n - base);
-        for (int j0 = 0; j0 < m; j0 += 4) {
-            float4 x[4][4];
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                w[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
-                if (j0 + u < m) {
-                    const float* src = o_base + static_cast<int64_t>(base + j0 + u) * piece_stride;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) x[u][v] = ld_f4(src + 4 * v);
-                } else {
-                    w[u] = 0.f;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    acc[4 * v + 0] += w[u] * x[u][v].x;
-                    acc[4 * v + 1] += w[u] * x[u][v].y;
-                    acc[4 * v + 2] += w[u] * x[u][v].z;
-                    acc[4 * v + 3] += w[u] * x[u][v].w;
-                }
-        }
     }
     const float inv = 1.f / wsum;
     uint32_t packed[8];
@@ -132,21 +172,34 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
+    // Warps per row from the average number of pieces per request (the plan
+    // has at most batch + parts pieces): when requests average eight pieces or
+    // more (few long sequences spread over many SM parts) eight warps share
+    // each row; otherwise one warp per row, four rows per CTA (measured: the
+    // wider form slowed steps whose requests have few pieces, its CTAs
+    // launching early beside the decode kernel).
+    const int parts = p.num_parts > 0 ? p.num_parts : 1;
+    const int avg = (p.batch + parts + p.batch - 1) / p.batch;
+    const int ki = avg >= 8 ? 1 : 0;
+    const int w = ki ? 8 : 1, warps = ki ? 8 : 4;
+    using Kernel = void (*)(CombineParams);
+    const Kernel kernels[2] = {combine_kernel<1, 4>, combine_kernel<8, 8>};
     // Same shared-memory carveout as the decode kernels (no SM reconfiguration
     // between the kernels of one step).
-    static int carveout_mask = 0;
+    static int carveout_mask[2] = {0, 0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 31 || !(__atomic_load_n(&carveout_mask, __ATOMIC_RELAXED) & (1 << dev))) {
-        e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    if (dev >= 31 || !(__atomic_load_n(&carveout_mask[ki], __ATOMIC_RELAXED) & (1 << dev))) {
+        e = cudaFuncSetAttribute(kernels[ki], cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        if (dev < 31) __atomic_fetch_or(&carveout_mask, 1 << dev, __ATOMIC_RELAXED);
+        if (dev < 31) __atomic_fetch_or(&carveout_mask[ki], 1 << dev, __ATOMIC_RELAXED);
     }
+    const int rows_per_cta = warps / w;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.R + kCombineWarps - 1) / kCombineWarps, p.batch, 1);
-    cfg.blockDim = dim3(32 * kCombineWarps, 1, 1);
+    cfg.gridDim = dim3((p.R + rows_per_cta - 1) / rows_per_cta, p.batch, 1);
+    cfg.blockDim = dim3(32 * warps, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -154,7 +207,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernels[ki], p);
 }
 
 }  // namespace mla

@@ -123,6 +123,7 @@ struct CombineParams {
     int64_t out_sb, out_ss, out_sh;
     float* lse;
     int batch, s_q, h_q, R;
+    int num_parts;  // SM parts of the plan (bounds the pieces: batch + num_parts)
     int fold;      // as DecodeParams::fold
     int kvh, grp;  // as DecodeParams::kvh, grp
 };
