@@ -239,7 +239,8 @@ int mla_set_decode_kernel(int kind) {
 int mla_get_decode_kernel(void) { return g_kernel.load(); }
 
 int mla_set_fixed_overhead(int blocks) {
-    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead : (blocks < 1 ? 1 : blocks));
+    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead
+                                      : (blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks)));
     return MLA_OK;
 }
 

@@ -188,9 +188,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return ok;
 }
 // Warp-uniform bounded wait of the leader's issuer warps on barriers whose
-// phases complete by remote arrivals from the peer: a thread suspended in
-// mbarrier.try_wait was measured to notice such a phase about a microsecond
-// late, so these poll with the non-suspending test_wait and a short sleep.
+// phases complete by remote arrivals from the peer.  It polls with the
+// non-suspending test_wait and a short sleep: measured against the suspending
+// try_wait on these barriers, the MTP step (batch 128, s_q 2, h_q 128, 4096
+// tokens) took 320 instead of 343 us and the ragged h_q 128 step 104 instead
+// of 108 us.
 __device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, const WaitCtx& wc) {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {

@@ -359,8 +359,9 @@ MLA_API int mla_set_wait_budget_ns(uint64_t budget_ns);
 /*
  * mla_set_fixed_overhead -- the scheduler's fixed per-piece overhead in
  * 64-token blocks (fixed_overhead_num_blocks in the "Tile Scheduler" section;
- * default 2, at least 1: 0 is raised to 1).  Affects only load balance, never
- * results.  Process-wide; negative restores the default.
+ * default 2; 0 is raised to 1 and values above 4096 are lowered to 4096).
+ * Affects only load balance, never results.  Process-wide; negative restores
+ * the default.
  */
 MLA_API int mla_set_fixed_overhead(int blocks);
 

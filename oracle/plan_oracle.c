@@ -17,18 +17,17 @@
  *   The per-part record has the fields of that section's DecodingSchedMeta.
  *
  * Readings of what the page leaves open:
- *   - Every request costs its blocks plus one fixed overhead c (c >= 1), so
- *     total = sum_i (n_i + c).  Lay the requests out in order on a line of
- *     cost units: request i owns c overhead units followed by its n_i block
- *     units.  Part p takes the next ceil(total / parts) units, the range
- *     [p * q, (p + 1) * q) with q = ceil(total / parts).
- *   - A request belongs to a part when the part's range holds at least one of
- *     its blocks; a request with no blocks belongs to the part holding its
- *     first overhead unit.  A part's record lists its first and last request
- *     and the block range it covers in each.
- *   - Cost of a part = sum over its pieces of (blocks + c) <= q + c = payload:
- *     the page's "+ fixed_overhead" is the room for the overhead a split
- *     request pays again in the part that continues it.
+ *   - total_num_blocks counts every request's blocks plus one fixed overhead
+ *     c (c >= 1): total = sum_i (n_i + c).  With blocks alone the cap could
+ *     not hold the overheads of a batch of many short requests.
+ *   - Every piece of a request costs its blocks plus c: a request continued
+ *     in a new part pays the overhead again there.
+ *   - The greedy walk, part by part with remain = payload: while requests are
+ *     left, if the rest of the current request (its unplaced blocks plus c)
+ *     fits in remain, the part takes it whole and moves to the next request;
+ *     otherwise the part takes remain - c blocks of it when that is at least
+ *     one block (the request continues in the next part) and the part is
+ *     closed.  Parts after the last request are empty.
  *   - begin/end request indices are inclusive, the begin block inclusive and
  *     the end block exclusive (the struct's comments on that page); an empty
  *     part has begin_req = b, end_req = b - 1, blocks 0..0.
@@ -46,76 +45,74 @@ enum { F_BEGIN_REQ, F_END_REQ, F_BEGIN_BLOCK, F_END_BLOCK, F_BEGIN_SPLIT, F_FIRS
 /*
  * oracle_plan: seqlens[b] -> parts[num_parts][8], num_splits[b + 1].
  * page is the KV page size in tokens; fixed_overhead >= 1.
- * Returns 0, or -3 on bad sizes, -2 out of memory.
+ * Returns 0, or -3 on bad sizes, -2 out of memory, -4 if the walk left work
+ * unplaced (the cap rules that out).
  */
 int oracle_plan(const int32_t *seqlens, int b, int page, int num_parts, int fixed_overhead,
                 int32_t *parts, int32_t *num_splits) {
     if (b < 1 || page <= 0 || num_parts <= 0 || fixed_overhead < 1) return -3;
     const int64_t c = fixed_overhead;
     int64_t *nblk = (int64_t *)malloc(sizeof(int64_t) * (size_t)b);
-    int64_t *start = (int64_t *)malloc(sizeof(int64_t) * (size_t)(b + 1));
     int32_t *pieces = (int32_t *)calloc((size_t)b, sizeof(int32_t));
     int32_t *first_piece_of_part = (int32_t *)malloc(sizeof(int32_t) * (size_t)num_parts);
-    if (!nblk || !start || !pieces || !first_piece_of_part) {
+    if (!nblk || !pieces || !first_piece_of_part) {
         free(nblk);
-        free(start);
         free(pieces);
         free(first_piece_of_part);
         return -2;
     }
-    /* step 1: blocks per request, and each request's place on the cost line */
-    start[0] = 0;
+    /* step 1: blocks per request, and the total they cost */
+    int64_t total = 0;
     for (int i = 0; i < b; ++i) {
         int64_t L = seqlens[i] > 0 ? seqlens[i] : 0;
         nblk[i] = (L + page - 1) / page;
-        start[i + 1] = start[i] + c + nblk[i];
+        total += nblk[i] + c;
     }
-    /* step 2: the share of one part */
-    const int64_t total = start[b];
-    const int64_t q = (total + num_parts - 1) / num_parts;
+    /* step 2: the cap of one part */
+    const int64_t payload = (total + num_parts - 1) / num_parts + c;
 
-    /* step 3: each part takes the next q units; requests in order */
+    /* step 3: the greedy walk, request by request */
+    int req = 0;     /* first request not yet fully placed */
+    int64_t blk = 0; /* its first unplaced block */
     for (int p = 0; p < num_parts; ++p) {
         int32_t *rec = parts + (int64_t)p * F_COUNT;
         for (int f = 0; f < F_COUNT; ++f) rec[f] = 0;
-        const int64_t a = (int64_t)p * q;
-        int64_t e = a + q;
-        if (e > total) e = total;
-        int first = -1, last = -1;
-        int64_t first_b0 = 0, last_b1 = 0;
-        for (int i = 0; i < b; ++i) {
-            const int64_t blk_lo = start[i] + c; /* line position of block 0 */
-            int in;
-            int64_t j0 = 0, j1 = 0;
-            if (nblk[i] > 0) {
-                j0 = a - blk_lo;
-                if (j0 < 0) j0 = 0;
-                j1 = e - blk_lo;
-                if (j1 > nblk[i]) j1 = nblk[i];
-                in = j1 > j0;
-            } else {
-                in = start[i] >= a && start[i] < e;
-            }
-            if (!in) continue;
-            if (first < 0) {
-                first = i;
-                first_b0 = j0;
-                first_piece_of_part[p] = pieces[i];
-            }
-            last = i;
-            last_b1 = j1;
-            pieces[i] += 1;
-        }
-        if (first < 0) {
+        if (req >= b) {
             rec[F_BEGIN_REQ] = b;
             rec[F_END_REQ] = b - 1;
             first_piece_of_part[p] = -1;
             continue;
         }
-        rec[F_BEGIN_REQ] = first;
-        rec[F_END_REQ] = last;
-        rec[F_BEGIN_BLOCK] = (int32_t)first_b0;
-        rec[F_END_BLOCK] = (int32_t)last_b1;
+        rec[F_BEGIN_REQ] = req;
+        rec[F_BEGIN_BLOCK] = (int32_t)blk;
+        first_piece_of_part[p] = pieces[req];
+        int64_t remain = payload;
+        while (req < b) {
+            const int64_t rest = nblk[req] - blk;
+            if (remain >= rest + c) { /* the rest fits: take it whole */
+                remain -= rest + c;
+                pieces[req] += 1;
+                rec[F_END_REQ] = req;
+                rec[F_END_BLOCK] = (int32_t)nblk[req];
+                req += 1;
+                blk = 0;
+                continue;
+            }
+            const int64_t take = remain - c; /* cut: as many blocks as fit */
+            if (take > 0) {
+                pieces[req] += 1;
+                rec[F_END_REQ] = req;
+                blk += take;
+                rec[F_END_BLOCK] = (int32_t)blk;
+            }
+            break;
+        }
+    }
+    if (req < b) { /* cannot happen: parts * payload covers every overhead paid */
+        free(nblk);
+        free(pieces);
+        free(first_piece_of_part);
+        return -4;
     }
 
     /* step 4: prefix sum of pieces per request */
@@ -133,7 +130,6 @@ int oracle_plan(const int32_t *seqlens, int b, int page, int num_parts, int fixe
         rec[F_LAST_SPLIT] = pieces[er] > 1;
     }
     free(nblk);
-    free(start);
     free(pieces);
     free(first_piece_of_part);
     return 0;

@@ -1,11 +1,12 @@
-"""The device tile scheduler (mla_get_metadata) against the oracle's plan:
-integer for integer, plus the plan invariants."""
+"""The device tile scheduler (mla_get_metadata) against the oracle's plan
+(the page's greedy walk): integer for integer, plus the plan invariants and
+the greedy-fill property."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from tests.test_plan_oracle import check_plan_invariants
+from tests.test_plan_oracle import check_greedy_fill, check_plan_invariants
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +56,7 @@ def test_device_plan_equals_oracle(seqlens, h_q, s_q):
     assert np.array_equal(ns, ref_ns)
     assert hdr[7] == ns[-1]
     check_plan_invariants(seqlens, parts, ns, num_parts, fixed)
+    check_greedy_fill(seqlens, parts, num_parts, fixed)
 
 
 def test_random_seqlens_plans():
@@ -67,3 +69,24 @@ def test_random_seqlens_plans():
         hdr, parts, ns = device_plan(seqlens, h_q, s_q)
         ref_parts, ref_ns = oracle.plan(seqlens, int(hdr[3]), int(hdr[5]))
         assert np.array_equal(parts, ref_parts) and np.array_equal(ns, ref_ns)
+        check_greedy_fill(seqlens, parts, int(hdr[3]), int(hdr[5]))
+
+
+@pytest.mark.parametrize("fixed", [1, 3, 9, 64])
+def test_fixed_overhead_and_many_requests(fixed):
+    """Many short requests (more requests than parts, parts closing at
+    boundaries and mid-request) under several overheads."""
+    from decode_attention_paged_gb300 import api
+
+    rng = np.random.default_rng(40 + fixed)
+    seqlens = rng.integers(0, 700, size=2000).tolist()
+    api.set_fixed_overhead(fixed)
+    try:
+        hdr, parts, ns = device_plan(seqlens, 16, 1)
+    finally:
+        api.set_fixed_overhead(-1)
+    assert int(hdr[5]) == fixed
+    ref_parts, ref_ns = oracle.plan(seqlens, int(hdr[3]), fixed)
+    assert np.array_equal(parts, ref_parts) and np.array_equal(ns, ref_ns)
+    check_plan_invariants(seqlens, parts, ns, int(hdr[3]), fixed)
+    check_greedy_fill(seqlens, parts, int(hdr[3]), fixed)
