@@ -106,7 +106,7 @@ constexpr uint32_t kOffKV = kOffQ + kQBytes;
 // (tmem base, abort flag, key masks).  The P buffer sits 8 KB-aligned right
 // after the ring: placed elsewhere the PV MMAs measured a few percent slower.
 constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kTailBytes = 256 + 2 * 128 * 8 + 64;
+constexpr uint32_t kTailBytes = 256 + 2 * 128 * 8 + 64 + 256;  // ..., block-table windows
 constexpr uint32_t kSmemBytes = kOffP + kTailBytes;             // P in each page's RoPE chunk
 constexpr uint32_t kSmemBytesP = kOffP + kPBytes + kTailBytes;  // with the P buffer
 static_assert(sizeof(Barriers) <= 256, "barrier block");
@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Barriers* bars = reinterpret_cast<Barriers*>(tail);
     uint2* xch = reinterpret_cast<uint2*>(tail + 256);
     uint8_t* misc = tail + 256 + 2 * 128 * 8;
+    int32_t* bt_win = reinterpret_cast<int32_t*>(misc + 64);  // int32 [2][32]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
     // Sparse decode: key_part[2 * stage + w] has bit t set when stage row t
@@ -374,9 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         // Loads run through a two-page ring.  The whole warp walks it (lane 0
-        // waits and issues the copies); block-table entries are loaded 32
-        // pages ahead, page g's by lane g % 32, and read with a shuffle when
-        // page g is issued, so a load never waits for its page index.
+        // waits and issues the copies).  Block-table entries come through two
+        // 32-page windows in shared memory: window w (pages 32w .. 32w + 31,
+        // page 32w + i copied by lane i with cp.async) is fetched while window
+        // w - 1 is in use, so no page waits for a global load (a load per page
+        // into a register would make the next page's read wait for it).
         //
         // Sparse decode: the gather warps fill the KV ring; this warp only
         // loads each request's Q tile.
@@ -384,19 +387,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
         const bool sparse = p.sparse != 0;
         Cursor ld = cursor_begin<kHeads>(p, part), ahead = ld;
-        int bid = 0;
-        if (!sparse) {
+        auto fetch_window = [&](uint32_t slot) {
+            int rq = -1, bk = 0;
             for (int i = 0; i < 32 && ahead.valid; ++i) {
-                if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req / kvh) * p.bt_stride +
-                                        ahead.blk];
+                if (lane == i) {
+                    rq = ahead.req;
+                    bk = ahead.blk;
+                }
                 cursor_next<kHeads>(p, part, ahead);
             }
-        }
+            if (rq >= 0)
+                cp_async_4(smem_u32(bt_win + 32 * slot + lane),
+                           p.block_table + static_cast<int64_t>(rq / kvh) * p.bt_stride + bk);
+            cp_async_commit();
+        };
         uint32_t n_kv = 0, n_q = 0;
+        // Q tile of request req (the whole tile, or its head-group slice).
+        auto issue_q = [&](int req) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+                if (!kHeads) {
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
+                                    mtile * kTileM, req, policy);
+                } else {
+                    // map (576, grp, h_kv, s_q, b): the tile's rows s * grp + hh of
+                    // head group j; a tile spans 64 / grp tokens, or one token's
+                    // 64-head slice when grp > 64.
+                    const int per_s = grp > kTileM ? grp / kTileM : 1;
+                    const int hh0 = grp > kTileM ? (mtile % per_s) * kTileM : 0;
+                    const int s0 = grp > kTileM ? mtile / per_s : mtile * (kTileM / grp);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_5d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c, hh0,
+                                    req % kvh, s0, req / kvh, policy);
+                }
+            }
+            __syncwarp();
+            ++n_q;
+        };
+        if (ld.valid) issue_q(ld.req);
+        if (!sparse) fetch_window(0);
         while (ld.valid) {
             if (!sparse) {
-                const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
+                // Window (g / 32) has landed: the first waits for its only
+                // group, later ones leave the next window's group pending.
+                if (ld.g == 0)
+                    cp_async_wait_group<0>();
+                else if ((ld.g & 31) == 0)
+                    cp_async_wait_group<1>();
+                __syncwarp();
+                const int page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
                 const int st = ld.g & 1;
                 if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
                 if (lane == 0) {
@@ -432,38 +472,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 ++n_kv;
             }
-            if (ld.blk == ld.b0) {  // first block of a request: its Q tile
-                if (ld.item > 0 && !warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-                    if (!kHeads) {
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
-                                        mtile * kTileM, ld.req, policy);
-                    } else {
-                        // map (576, grp, h_kv, s_q, b): the tile's rows s * grp + hh
-                        // of head group j; a tile spans 64 / grp tokens, or one
-                        // token's 64-head slice when grp > 64.
-                        const int per_s = grp > kTileM ? grp / kTileM : 1;
-                        const int hh0 = grp > kTileM ? (mtile % per_s) * kTileM : 0;
-                        const int s0 = grp > kTileM ? mtile / per_s : mtile * (kTileM / grp);
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_5d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c, hh0,
-                                        ld.req % kvh, s0, ld.req / kvh, policy);
-                    }
-                }
-                __syncwarp();
-                ++n_q;
+            // First block of a request: its Q tile (the part's first one went
+            // out before the loop).
+            if (ld.blk == ld.b0 && ld.g > 0) {
+                if (!warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
+                issue_q(ld.req);
             }
-            // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
-            if (!sparse && ahead.valid) {
-                if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req / kvh) * p.bt_stride +
-                                        ahead.blk];
-                cursor_next<kHeads>(p, part, ahead);
+            // After page 0: the second window; after the last page of window
+            // w: window w + 2 into w's slot (every lane has read its entry).
+            if (!sparse) {
+                if (ld.g == 0)
+                    fetch_window(1);
+                else if ((ld.g & 31) == 31)
+                    fetch_window((ld.g >> 5) & 1);
             }
             cursor_next<kHeads>(p, part, ld);
         }
+        cp_async_wait_all();
         // Drain: never leave the CTA with copies still landing in its smem.
         if (lane == 0) {
             for (uint32_t k = (n_kv >= 2 ? n_kv - 2 : 0); k < n_kv; ++k)

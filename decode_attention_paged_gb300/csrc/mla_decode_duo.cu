@@ -51,8 +51,10 @@
 // sub-partition) each take 16 tokens of a row: warp w reads TMEM lane quadrant
 // w % 4 (rows and rail) and token half w / 4.  P goes into slot 4 of the
 // page's stage, which QK^T is done with (the peer's producer zeroes it again
-// before the stage's next page).  The peer's softmax warps signal the leader
-// through two relay warps (one remote arrival per page).  Every wait is
+// before the stage's next page).  The peer's softmax warps signal the leader's
+// issuers with relaxed remote arrivals, one per warp and page (measured: a
+// relay warp forwarding one arrival per page made the MTP step 12% and the
+// ragged h_q 128 step 7% slower).  Every wait is
 // bounded; after a timeout the softmax warps still pass every named barrier,
 // and the two CTAs meet at a cluster barrier before tensor memory is freed.
 #include "mla_internal.h"
@@ -64,9 +66,8 @@ namespace {
 
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kPvWarp = 10;      // the leader's PV issuer
-constexpr int kRelayWarp0 = 10;  // warps 10, 11: the peer's relays
-constexpr int kThreads = 384;
+constexpr int kPvWarp = 10;  // the leader's PV issuer (idle in the peer)
+constexpr int kThreads = 352;
 constexpr int kPairRows = 128;  // query rows of one CTA pair
 constexpr int kCtaRows = 64;    // rows of one CTA
 constexpr int kStages = 5;
@@ -81,7 +82,8 @@ constexpr uint32_t kOffM = kOffX + kXBytes;  // row max / row sum exchange: floa
 constexpr uint32_t kMBytes = 2 * 4 * 64 * 4;
 constexpr uint32_t kOffBar = kOffM + kMBytes;
 constexpr uint32_t kOffMisc = kOffBar + 256;
-constexpr uint32_t kSmemBytes = kOffMisc + 64;
+constexpr uint32_t kOffBt = kOffMisc + 64;  // block-table windows: int32 [2][32]
+constexpr uint32_t kSmemBytes = kOffBt + 256;
 static_assert(kOffQr % 1024 == 0 && kOffX % 16 == 0, "operand alignment");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
 static_assert(kSmemBytes < (1u << 18), "descriptor address arithmetic assumes < 256 KB");
@@ -109,15 +111,13 @@ struct Barriers {
     uint64_t kv_peer[kStages];   // leader: the peer's half of a page landed
     uint64_t kv_empty[kStages];  // this CTA's stage may be refilled
     uint64_t s_full[2];          // S of a page is in this CTA's TMEM
-    uint64_t s_empty[2];         // leader: both CTAs' softmax warps have read S
-    uint64_t p_full[2];          // leader: both CTAs' softmax warps wrote P (and rescaled O)
+    uint64_t s_empty[2];         // leader: all 16 softmax warps have read S
+    uint64_t p_full[2];          // leader: all 16 softmax warps wrote P (and rescaled O)
     uint64_t pv_done[2];         // PV of a page finished (both CTAs)
     uint64_t q_ready;            // leader: both CTAs copied a request's Q
     uint64_t o_free;             // leader: all 16 softmax warps read O in the epilogue
     uint64_t drain;              // leader: every MMA of both issuers finished
     uint64_t q_copied;           // peer: its softmax warps copied a request's Q (entries landed)
-    uint64_t s_relay[2];         // peer: its 8 softmax warps read S (relayed to s_empty)
-    uint64_t p_relay[2];         // peer: its 8 softmax warps wrote P (relayed to p_full)
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 
@@ -272,10 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->s_full[b], 1);
-            mbar_init(&bars->s_empty[b], 9);  // 8 leader warps + the peer's relay
-            mbar_init(&bars->p_full[b], 9);
-            mbar_init(&bars->s_relay[b], 8);
-            mbar_init(&bars->p_relay[b], 8);
+            mbar_init(&bars->s_empty[b], 16);  // the softmax warps of both CTAs
+            mbar_init(&bars->p_full[b], 16);
             mbar_init(&bars->pv_done[b], 1);
         }
         mbar_init(&bars->q_ready, 2);
@@ -334,18 +332,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         // The whole warp walks the ring; lane 0 waits and issues the copies.
-        // Block-table entries are loaded 32 pages ahead, page g's by lane
-        // g % 32, and read with a shuffle when page g is issued.
+        // Block-table entries come through two 32-page windows in shared
+        // memory: window w (pages 32w .. 32w + 31, page 32w + i copied by
+        // lane i with cp.async) is fetched while window w - 1 is in use, so
+        // no page waits for a global load (a load per page into a register
+        // would make the next page's read wait for it).
         const uint64_t policy = policy_evict_first();
         const int qrow0 = tile * kPairRows + static_cast<int>(rank) * kCtaRows;
         const int n_kv = leader ? 5 : 4;
+        int32_t* bt_win = reinterpret_cast<int32_t*>(smem + kOffBt);
         Cursor ld = cursor_begin(p, part), ahead = ld;
-        int bid = 0;
-        for (int i = 0; i < 32 && ahead.valid; ++i) {
-            if (lane == static_cast<int>(ahead.g & 31))
-                bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-            cursor_next(p, part, ahead);
-        }
+        auto fetch_window = [&](uint32_t slot) {
+            int rq = -1, bk = 0;
+            for (int i = 0; i < 32 && ahead.valid; ++i) {
+                if (lane == i) {
+                    rq = ahead.req;
+                    bk = ahead.blk;
+                }
+                cursor_next(p, part, ahead);
+            }
+            if (rq >= 0)
+                cp_async_4(smem_u32(bt_win + 32 * slot + lane),
+                           p.block_table + static_cast<int64_t>(rq) * p.bt_stride + bk);
+            cp_async_commit();
+        };
+        fetch_window(0);
         uint32_t n_issued = 0;
         bool stop = false;
         auto acquire = [&](uint32_t n) -> bool {
@@ -353,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    warp_wait(&bars->kv_empty[n % kStages], ((n / kStages) + 1) & 1, wc);
         };
         while (ld.valid && !stop) {
-            const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
             if (ld.blk == ld.b0) {
                 // The request's 64 query rows of this CTA: chunks 0, 1, 4, 5 and
                 // the RoPE chunk, then chunks 2, 3, 6, 7.
@@ -378,6 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (stop) break;
             }
+            // Window (g / 32) has landed: the first waits for its only group,
+            // later ones leave the next window's group pending.
+            if (ld.g == 0)
+                cp_async_wait_group<0>();
+            else if ((ld.g & 31) == 0)
+                cp_async_wait_group<1>();
+            __syncwarp();
+            const int page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
             const uint32_t n = ld.ring();
             const uint32_t st = n % kStages;
             if (!acquire(n)) break;
@@ -400,15 +418,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             n_issued = n + 1;
-            // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
-            if (ahead.valid) {
-                if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-                cursor_next(p, part, ahead);
-            }
+            // After page 0: the second window; after the last page of window
+            // w: window w + 2 into w's slot (every lane has read its entry).
+            if (ld.g == 0)
+                fetch_window(1);
+            else if ((ld.g & 31) == 31)
+                fetch_window((ld.g >> 5) & 1);
             cursor_next(p, part, ld);
         }
         // Drain: no copy may still be landing when the CTA leaves.
+        cp_async_wait_all();
         if (lane == 0)
             for (uint32_t k = (n_issued >= kStages ? n_issued - kStages : 0); k < n_issued; ++k)
                 mbar_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, kDrainBudgetNs);
@@ -530,14 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (alive) alive = warp_wait(bar, parity, wc);
             return alive;
         };
-        // Per-page signals to the leader's MMA warp: local arrivals in the
-        // leader; in the peer, arrivals on local relay barriers that the
-        // relay warps forward (a remote arrival costs this warp a few hundred
-        // nanoseconds).
-        auto signal = [&](uint64_t* leader_bar, uint64_t* relay_bar) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(leader ? leader_bar : relay_bar);
-        };
+        // Per-page signals to the leader's issuers: one arrival per warp,
+        // remote (relaxed) from the peer.
+        auto signal = [&](uint64_t* leader_bar) { warp_arrive_leader(leader_bar, leader); };
         // PV completions are observed in page order, and before P(g) is written
         // PV(g - 2) must be complete: a parity wait on pv_done[g & 1] is only
         // unambiguous when PV(g - 2) is known complete and PV(g + 2) cannot be
@@ -620,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) sv[c] = 0u;
                 }
-                signal(&bars->s_empty[sbuf], &bars->s_relay[sbuf]);
+                signal(&bars->s_empty[sbuf]);
                 // Keep tokens [32h + 16 rho, +16); hand the other 16 to the
                 // thread of the other rail (lane Lr ^ 64, same h).  rho is
                 // uniform over the warp, so each branch indexes statically.
@@ -739,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                signal(&bars->p_full[sbuf], &bars->p_relay[sbuf]);
+                signal(&bars->p_full[sbuf]);
             }
             if (has_blocks) {
                 // The next request with blocks: its query entries follow this
@@ -826,20 +840,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     p.lse[om.lse_idx] = empty ? -INFINITY : lse2 * 0.69314718055994531f;
             }
-        }
-    } else if (!leader && warp >= kRelayWarp0) {
-        // -------------------------------------------------- peer: relay warps
-        // Forward, page by page, this CTA's "S read" (warp 10) and "P written"
-        // (warp 11) to the leader's barriers: one remote arrival per page
-        // instead of one per softmax warp.  In page order, which keeps each
-        // parity wait unambiguous (the next phase of a relay barrier needs the
-        // leader to have acted on this one).
-        uint64_t* relay = warp == kRelayWarp0 ? bars->s_relay : bars->p_relay;
-        uint64_t* target = warp == kRelayWarp0 ? bars->s_empty : bars->p_full;
-        for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
-            if (!warp_wait(&relay[c.g & 1], (c.g >> 1) & 1, wc)) break;
-            if (lane == 0) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&target[c.g & 1]), 0));
-            __syncwarp();
         }
     }
 

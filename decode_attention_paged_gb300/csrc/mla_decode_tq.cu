@@ -89,7 +89,7 @@ static_assert(sizeof(Barriers) <= 256, "barrier block");
 // are padding rows whose scores the softmax masks), then the KV stages.
 struct TqLayout {
     uint32_t q_rows, n_stages;
-    uint32_t off_kv, off_v, off_bar, off_misc, bytes;
+    uint32_t off_kv, off_v, off_bar, off_misc, off_bt, bytes;
 };
 __host__ __device__ constexpr TqLayout tq_layout(int q_box_rows) {
     TqLayout l{};
@@ -99,7 +99,8 @@ __host__ __device__ constexpr TqLayout tq_layout(int q_box_rows) {
     l.off_v = l.off_kv + l.n_stages * kStageBytes;  // row max / row sum swap: float[128]
     l.off_bar = l.off_v + 512u;
     l.off_misc = l.off_bar + 256u;  // tmem base, abort flag
-    l.bytes = l.off_misc + 64u;
+    l.off_bt = l.off_misc + 64u;    // block-table windows: int32 [2][32]
+    l.bytes = l.off_bt + 256u;
     return l;
 }
 static_assert(tq_layout(32).n_stages == 3 && tq_layout(64).n_stages == 2, "stage counts");
@@ -287,12 +288,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         // The whole warp walks the ring; lane 0 waits and issues the copies.
-        // Block-table entries are loaded 32 pages ahead, page g's by lane
-        // g % 32, and read with a shuffle when page g is issued: the load has
-        // long landed by then, so the producer never stalls on it.
+        // Block-table entries come through two 32-page windows in shared
+        // memory: window w (pages 32w .. 32w + 31, page 32w + i copied by
+        // lane i with cp.async) is fetched while window w - 1 is in use, so
+        // no page waits for a global load (a load per page into a register
+        // would make the next page's read wait for it).
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
+        int32_t* bt_win = reinterpret_cast<int32_t*>(smem + lay.off_bt);
         Cursor ld = cursor_begin(p, part), ahead = ld;
+        auto fetch_window = [&](uint32_t slot) {
+            int rq = -1, bk = 0;
+            for (int i = 0; i < 32 && ahead.valid; ++i) {
+                if (lane == i) {
+                    rq = ahead.req;
+                    bk = ahead.blk;
+                }
+                cursor_next(p, part, ahead);
+            }
+            if (rq >= 0)
+                cp_async_4(smem_u32(bt_win + 32 * slot + lane),
+                           p.block_table + static_cast<int64_t>(rq) * p.bt_stride + bk);
+            cp_async_commit();
+        };
         uint32_t n_issued = 0;  // ring entries issued
         // The first request's Q tile (ring entry 0) needs no block-table entry:
         // it goes out before the look-ahead loads.
@@ -306,15 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             n_issued = 1;
         }
-        int bid = 0;
-        for (int i = 0; i < 32 && ahead.valid; ++i) {
-            if (lane == static_cast<int>(ahead.g & 31))
-                bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-            cursor_next(p, part, ahead);
-        }
+        fetch_window(0);
         bool stop = false;
         while (ld.valid && !stop) {
-            const int page = __shfl_sync(0xffffffffu, bid, ld.g & 31);
             // First block of a request: its Q tile goes into the ring first
             // (already out for the part's first request).
             for (int entry = (ld.blk == ld.b0 && ld.g > 0) ? 0 : 1; entry < 2; ++entry) {
@@ -323,6 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (n >= n_stages && !warp_wait(&bars->kv_empty[st], ((n / n_stages) + 1) & 1, wc)) {
                     stop = true;
                     break;
+                }
+                int page = 0;
+                if (entry == 1) {
+                    // Window (g / 32) has landed: the first waits for its only
+                    // group, later ones leave the next window's group pending.
+                    if (ld.g == 0)
+                        cp_async_wait_group<0>();
+                    else if ((ld.g & 31) == 0)
+                        cp_async_wait_group<1>();
+                    __syncwarp();
+                    page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
                 }
                 if (lane == 0) {
                     uint8_t* dst = sKV + st * kStageBytes;
@@ -342,14 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n_issued = n + 1;
             }
             if (stop) break;
-            // Lane ld.g % 32 has handed out its entry; it loads page ld.g + 32.
-            if (ahead.valid) {
-                if (lane == static_cast<int>(ahead.g & 31))
-                    bid = p.block_table[static_cast<int64_t>(ahead.req) * p.bt_stride + ahead.blk];
-                cursor_next(p, part, ahead);
-            }
+            // After page 0: the second window; after the last page of window
+            // w: window w + 2 into w's slot (every lane has read its entry).
+            if (ld.g == 0)
+                fetch_window(1);
+            else if ((ld.g & 31) == 31)
+                fetch_window((ld.g >> 5) & 1);
             cursor_next(p, part, ld);
         }
+        cp_async_wait_all();
         if (lane == 0)
             for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k)
                 mbar_drain(&bars->kv_full[k % n_stages], (k / n_stages) & 1, kDrainBudgetNs);
