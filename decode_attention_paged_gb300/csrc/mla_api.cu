@@ -721,8 +721,12 @@ int mla_decode_fp8_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
     p.kvh = 1;
     p.grp = h_q;
-    // (The kernel takes a page tensor map too; the FP8 path never reads it.)
-    cudaError_t e = launch_decode(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream));
+    // The kernel that keeps Q in tensor memory (three stages) where the dense
+    // path would use it, else the single-CTA kernel.  (Both take a page
+    // tensor map too; the FP8 path never reads it.)
+    const bool tq = kernel_for(R, 1, d) == MLA_KERNEL_TQ;
+    cudaError_t e = tq ? launch_decode_tq(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream))
+                       : launch_decode(p, q_map, q_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, R, parts,
                         s_q, h_q, 0, 1, h_q, out_dev, out_batch_stride, out_s_stride,

@@ -49,6 +49,7 @@
 // early exit through a barrier reduction, so they always pass the same
 // barriers.  Every wait is bounded; a timeout records MLA_ERR_DEVICE_TIMEOUT,
 // drains the CTA's own copies and MMAs, frees TMEM and returns.
+#include "mla_fp8.cuh"
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -59,7 +60,10 @@ namespace {
 constexpr int kProducerWarp = 4;
 constexpr int kQkWarp = 5;
 constexpr int kPvWarp = 7;
+constexpr int kDequantWarp0 = 8;  // FP8 cache: warps 8..15 dequantise each page
 constexpr int kThreads = 256;
+constexpr int kThreadsFp8 = 512;
+constexpr uint32_t kDequantBar = 3;  // named barrier of the eight dequant warps
 
 constexpr int kMaxStages = 3;
 constexpr uint32_t kStageBytes = kChunks * kChunkBytes;  // 73728
@@ -80,6 +84,7 @@ struct Barriers {
     uint64_t p_full[2], pv_done[2];  // by page parity
     uint64_t o_free;
     uint64_t drain_qk, drain_pv;
+    uint64_t raw_full[kMaxStages];  // FP8: a ring entry's raw rows landed (Q entries: at issue)
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 
@@ -98,7 +103,7 @@ __host__ __device__ constexpr TqLayout tq_layout(int q_box_rows) {
     l.off_kv = 2u * l.q_rows * 128u;  // a multiple of 1024
     l.off_v = l.off_kv + l.n_stages * kStageBytes;  // row max / row sum swap: float[128]
     l.off_bar = l.off_v + 512u;
-    l.off_misc = l.off_bar + 256u;  // tmem base, abort flag
+    l.off_misc = l.off_bar + 256u;  // tmem base, abort flag, FP8 out-of-cache flags
     l.off_bt = l.off_misc + 64u;    // block-table windows: int32 [2][32]
     l.bytes = l.off_bt + 256u;
     return l;
@@ -197,7 +202,12 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+// kFp8: the cache is in the FP8 layout ("[DeepSeek-3] FlashMLA", sec. 12).
+// Each page's raw rows (one bulk copy) land at the top of its stage and eight
+// more warps dequantise them in place into the bf16 page the MMAs read
+// (mla_fp8.cuh, four threads per row); Q entries are bf16 as always.
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     decode_tq_kernel(const __grid_constant__ DecodeParams p,
                      const __grid_constant__ CUtensorMap q_map,
                      const __grid_constant__ CUtensorMap kv_map) {
@@ -218,14 +228,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     Barriers* bars = reinterpret_cast<Barriers*>(smem + lay.off_bar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.off_misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.off_misc + 4);
+    volatile int* raw_bad = reinterpret_cast<volatile int*>(smem + lay.off_misc + 8);  // [3]
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
     if (tid == 0) {
         *abort_flag = 0;
         for (uint32_t s = 0; s < n_stages; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
+            // FP8: a page is full when the eight dequant warps arrived; a Q
+            // entry gets its eight arrivals from the producer.
+            mbar_init(&bars->kv_full[s], kFp8 ? 8 : 1);
             mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->raw_full[s], 1);
         }
         mbar_init(&bars->q_ready, n_active);
         mbar_init(&bars->s_full, 1);
@@ -312,16 +326,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_commit();
         };
         uint32_t n_issued = 0;  // ring entries issued
+        uint32_t page_bits = 0;  // bit s: stage s's last entry was a page
+        // Q tile of request req into stage st.  (FP8: the producer also makes
+        // the dequant warps' seven other arrivals and completes the entry's
+        // raw_full phase, which keeps that barrier's phases in ring order.)
+        auto issue_q = [&](uint32_t st, int req) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->kv_full[st], q_bytes);
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(&q_map, &bars->kv_full[st], sKV + st * kStageBytes + c * kChunkBytes,
+                                64 * c, mtile * kTileM, req, policy);
+                if (kFp8) {
+                    for (int k = 0; k < 7; ++k) mbar_arrive(&bars->kv_full[st]);
+                    mbar_arrive(&bars->raw_full[st]);
+                }
+            }
+            __syncwarp();
+            page_bits &= ~(1u << st);
+        };
         // The first request's Q tile (ring entry 0) needs no block-table entry:
         // it goes out before the look-ahead loads.
         if (ld.valid) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->kv_full[0], q_bytes);
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(&q_map, &bars->kv_full[0], sKV + c * kChunkBytes, 64 * c,
-                                mtile * kTileM, ld.req, policy);
-            }
-            __syncwarp();
+            issue_q(0, ld.req);
             n_issued = 1;
         }
         fetch_window(0);
@@ -347,21 +373,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
                 }
-                if (lane == 0) {
-                    uint8_t* dst = sKV + st * kStageBytes;
-                    if (entry == 0) {
-                        mbar_arrive_expect_tx(&bars->kv_full[st], q_bytes);
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(&q_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
-                                        mtile * kTileM, ld.req, policy);
-                    } else {
-                        mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                        for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes, 64 * c,
-                                        0, page, policy);
+                if (entry == 0) {
+                    issue_q(st, ld.req);
+                } else {
+                    if (lane == 0) {
+                        uint8_t* dst = sKV + st * kStageBytes;
+                        if (kFp8) {
+                            // One copy of the page's raw rows; a page outside
+                            // the cache is not read and dequantises to zeros
+                            // (as the bf16 tile reads zeros out of range).
+                            const bool in =
+                                page >= 0 && static_cast<int64_t>(page) * kPage < p.num_tokens;
+                            raw_bad[st] = in ? 0 : 1;
+                            if (in) {
+                                mbar_arrive_expect_tx(&bars->raw_full[st], kFp8PageBytes);
+                                bulk_load(dst + kFp8RawOff,
+                                          p.kv_bytes + static_cast<int64_t>(page) * p.kv_page_bytes,
+                                          kFp8PageBytes, &bars->raw_full[st], policy);
+                            } else {
+                                mbar_arrive(&bars->raw_full[st]);
+                            }
+                        } else {
+                            mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                            for (int c = 0; c < kChunks; ++c)
+                                tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes,
+                                            64 * c, 0, page, policy);
+                        }
                     }
+                    __syncwarp();
+                    page_bits |= 1u << st;
                 }
-                __syncwarp();
                 n_issued = n + 1;
             }
             if (stop) break;
@@ -374,9 +415,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             cursor_next(p, part, ld);
         }
         cp_async_wait_all();
+        // Drain: no copy may still be landing when the CTA leaves (an FP8
+        // page's copy completes raw_full; everything else kv_full).
         if (lane == 0)
-            for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k)
-                mbar_drain(&bars->kv_full[k % n_stages], (k / n_stages) & 1, kDrainBudgetNs);
+            for (uint32_t k = (n_issued >= n_stages ? n_issued - n_stages : 0); k < n_issued; ++k) {
+                const uint32_t st = k % n_stages;
+                const bool raw = kFp8 && ((page_bits >> st) & 1u);
+                mbar_drain(raw ? &bars->raw_full[st] : &bars->kv_full[st], (k / n_stages) & 1,
+                           kDrainBudgetNs);
+            }
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------ QK^T issuer
@@ -458,6 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_drain(&bars->drain_pv, 0, kDrainBudgetNs);
         __syncwarp();
+    } else if (kFp8 && warp >= kDequantWarp0) {
+        // ---------------------------------------- FP8 page dequantisation
+        // In place, four threads per row (mla_fp8.cuh); the eight warps agree
+        // on every exit through bar.red.and before the named barrier inside
+        // the routine.  A page's raw_full phase is unambiguous: the stage's
+        // previous entry completed its phase before this page was issued
+        // into the stage, and the next cannot start before this page's PV.
+        const int dt = tid - 32 * kDequantWarp0;
+        for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
+            const uint32_t n = c.ring(), st = n % n_stages;
+            const bool ok = warp_wait(&bars->raw_full[st], (n / n_stages) & 1, wc);
+            if (!named_bar_and(kDequantBar, 256, ok)) break;
+            fp8_dequant_page_x4(sKV + st * kStageBytes, dt, raw_bad[st] != 0, kDequantBar);
+            fence_proxy_async_smem();
+            warp_arrive(&bars->kv_full[st]);
+        }
     } else if (softmax_warp) {
         // ---------------- softmax / correction / epilogue / Q copy
         const int q4 = warp;              // TMEM lane quadrant
@@ -755,13 +818,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
+template <bool kFp8>
 static cudaError_t tq_set_smem() {
     static int configured_mask = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(__atomic_load_n(&configured_mask, __ATOMIC_RELAXED) & (1 << dev))) {
-        e = cudaFuncSetAttribute(decode_tq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_tq_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemMax));
         if (e != cudaSuccess) return e;
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
@@ -771,11 +835,12 @@ static cudaError_t tq_set_smem() {
 
 cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
                              const CUtensorMap& kv_map, cudaStream_t stream) {
-    cudaError_t e = tq_set_smem();
+    const bool fp8 = p.fp8 != 0;
+    cudaError_t e = fp8 ? tq_set_smem<true>() : tq_set_smem<false>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_mtiles, p.num_parts, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(fp8 ? kThreadsFp8 : kThreads, 1, 1);
     cfg.dynamicSmemBytes = tq_layout(p.q_box_rows).bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -783,7 +848,8 @@ cudaError_t launch_decode_tq(const DecodeParams& p, const CUtensorMap& q_map,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tq_kernel, p, q_map, kv_map);
+    return fp8 ? cudaLaunchKernelEx(&cfg, decode_tq_kernel<true>, p, q_map, kv_map)
+               : cudaLaunchKernelEx(&cfg, decode_tq_kernel<false>, p, q_map, kv_map);
 }
 
 }  // namespace mla

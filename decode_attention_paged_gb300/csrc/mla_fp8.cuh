@@ -81,4 +81,56 @@ __device__ __forceinline__ void fp8_dequant_page(uint8_t* stage, int dt, bool ba
             bad ? make_uint4(0, 0, 0, 0) : rope[u];
 }
 
+// The same page with 256 threads (dt = 0..255), four per row: thread (t, q)
+// takes latent dims [128 q, 128 q + 128) with their scale and RoPE dims
+// [16 q, 16 q + 16); the 16-byte reads of a row's four threads start at
+// rotated units so that the eight threads of a quarter warp hit distinct
+// bank groups.  Same rounding and the same barrier rule as above.  The unit
+// loop is not unrolled (the staged units move down one register slot per
+// turn): measured, the smaller code ran the page about 1% faster than the
+// unrolled loop, and eight warps in place of four took the FP8 memory-bound
+// step from 111 to 93 us.
+__device__ __forceinline__ void fp8_dequant_page_x4(uint8_t* stage, int dt, bool bad,
+                                                    uint32_t bar_id) {
+    const int t = dt >> 2, q = dt & 3;
+    const uint8_t* raw = stage + kFp8RawOff + t * kFp8RowBytes;
+    uint4 lat[8], rope[2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        lat[k] = *reinterpret_cast<const uint4*>(raw + 128 * q + 16 * ((k + 2 * q) & 7));
+#pragma unroll
+    for (int k = 0; k < 2; ++k) rope[k] = *reinterpret_cast<const uint4*>(raw + 528 + 32 * q + 16 * k);
+    const float sc = *reinterpret_cast<const float*>(raw + 512 + 4 * q);
+    named_bar_sync(bar_id, 256);
+    uint64_t s2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(sc));
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+        const int u = (k + 2 * q) & 7;  // 16-dim unit of this thread's 128 dims
+        const uint32_t in[4] = {lat[0].x, lat[0].y, lat[0].z, lat[0].w};
+#pragma unroll
+        for (int i = 0; i < 7; ++i) lat[i] = lat[i + 1];
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const __nv_fp8x2_storage_t two =
+                static_cast<__nv_fp8x2_storage_t>(in[j >> 1] >> (16 * (j & 1)));
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            o[j] = bad ? 0u : mul2_pack_bf16x2(f.x, f.y, s2);
+        }
+        const int dim0 = 128 * q + 16 * u;
+        uint8_t* chunk = stage + (dim0 >> 6) * 8192;
+        const uint32_t unit = (dim0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(chunk + sw128_offset(t, unit + 1)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    uint8_t* rchunk = stage + 8 * 8192;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        *reinterpret_cast<uint4*>(rchunk + sw128_offset(t, 2 * q + k)) =
+            bad ? make_uint4(0, 0, 0, 0) : rope[k];
+}
+
 }  // namespace mla

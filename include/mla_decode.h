@@ -273,7 +273,10 @@ MLA_API int mla_decode_fwd_noalloc(const void *q_dev, int64_t q_batch_stride,
  *                apart (>= 41984, a multiple of 16); 16-byte aligned.  A
  *                block-table entry outside [0, num_pages) reads zeros.
  *   everything else as mla_decode_fwd; the metadata from mla_get_metadata.
- * Always runs the single-CTA kernel (its plan is the same as the TQ kernel's).
+ * Runs the kernel that keeps most of Q in tensor memory where mla_decode_fwd
+ * would (s_q * h_q <= 32 by default, or as mla_set_decode_kernel chose), with
+ * four more warps that dequantise each page in shared memory; otherwise the
+ * single-CTA kernel, which runs any plan mla_get_metadata made.
  * Enqueues the decode kernel and the combine kernel on `stream`;
  * graph-capturable.
  */

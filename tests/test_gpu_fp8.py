@@ -1,7 +1,8 @@
 """Decode over an FP8-layout cache ("[DeepSeek-3] FlashMLA", sec. 12: 656-byte
 rows of e4m3 latent values, fp32 scales and bf16 RoPE, dequantised to bf16) on
 the GPU against the fp64 oracle (dense decode over the dequantised rows),
-element by element.  Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|,
+element by element, on both kernels that read it (the single-CTA one and the
+one that keeps Q in tensor memory).  Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|,
 |lse - ref| <= 1e-3."""
 import numpy as np
 import pytest
@@ -44,8 +45,19 @@ def ref_fp8(w):
                                  nthreads=NTHREADS)
 
 
+@pytest.fixture
+def kernel_kind(request):
+    from decode_attention_paged_gb300 import api
+
+    default = api.get_decode_kernel()
+    api.set_decode_kernel(request.param)
+    yield request.param
+    api.set_decode_kernel(default)
+
+
+@pytest.mark.parametrize("kernel_kind", [3, 1, 2], indirect=True, ids=["auto", "single", "tq"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
-def test_fp8_parity(case):
+def test_fp8_parity(kernel_kind, case):
     b, s_q, h_q, seqlens, causal = case
     w = W.as_fp8(W.random_case(800 + CASES.index(case), b, s_q, h_q, seqlens, causal))
     out, lse = run_fp8(w)
