@@ -22,11 +22,23 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
-constexpr int kDefaultFixedOverhead = 2;
+// The scheduler's fixed overhead per request piece, in 64-token blocks, by
+// kernel: what a request boundary measured costs each kernel in pages of
+// streaming (sweeps of 1..8 on GB300: the single-CTA kernel best at 2, the
+// tensor-memory-Q kernel at 4, the CTA-pair kernel at 5-6).  A value set with
+// mla_set_fixed_overhead overrides them.
+int default_fixed_overhead(int kind) {
+    return kind == MLA_KERNEL_DUO ? 5 : (kind == MLA_KERNEL_TQ ? 4 : 2);
+}
 
 std::atomic<uint64_t> g_budget_ns{kDefaultBudgetNs};
-std::atomic<int> g_fixed_overhead{kDefaultFixedOverhead};
+std::atomic<int> g_fixed_overhead{-1};  // -1: the kernel's default
 std::atomic<int> g_kernel{MLA_KERNEL_AUTO};
+
+int fixed_overhead_for(int kind) {
+    const int v = g_fixed_overhead.load();
+    return v >= 1 ? v : default_fixed_overhead(kind);
+}
 
 struct DeviceInfo {
     std::once_flag once;
@@ -239,8 +251,7 @@ int mla_set_decode_kernel(int kind) {
 int mla_get_decode_kernel(void) { return g_kernel.load(); }
 
 int mla_set_fixed_overhead(int blocks) {
-    g_fixed_overhead.store(blocks < 0 ? kDefaultFixedOverhead
-                                      : (blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks)));
+    g_fixed_overhead.store(blocks < 0 ? -1 : (blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks)));
     return MLA_OK;
 }
 
@@ -270,7 +281,8 @@ int mla_get_metadata(const int32_t* cache_seqlens_dev, int batch, int h_q, int s
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     const int parts = num_parts_of(g.R, h_kv, d);
     cudaError_t e = launch_sched(cache_seqlens_dev, h_kv, -1, g.nreq, g.R, parts,
-                                 tiles_of(g.R, kernel_for(g.R, h_kv, d)), g_fixed_overhead.load(),
+                                 tiles_of(g.R, kernel_for(g.R, h_kv, d)),
+                                 fixed_overhead_for(kernel_for(g.R, h_kv, d)),
                                  static_cast<int32_t*>(meta_dev), num_splits_dev,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -535,7 +547,7 @@ int mla_get_metadata_sparse(int topk, int batch, int h_q, int s_q, int h_kv, voi
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     cudaError_t e = launch_sched(nullptr, 1, topk, batch * s_q, h_q, num_parts_single(h_q, d),
-                                 n_mtiles_of(h_q), g_fixed_overhead.load(),
+                                 n_mtiles_of(h_q), fixed_overhead_for(MLA_KERNEL_SINGLE),
                                  static_cast<int32_t*>(meta_dev), num_splits_dev,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

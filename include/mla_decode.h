@@ -362,9 +362,11 @@ MLA_API int mla_set_wait_budget_ns(uint64_t budget_ns);
 /*
  * mla_set_fixed_overhead -- the scheduler's fixed per-piece overhead in
  * 64-token blocks (fixed_overhead_num_blocks in the "Tile Scheduler" section;
- * default 2; 0 is raised to 1 and values above 4096 are lowered to 4096).
- * Affects only load balance, never results.  Process-wide; negative restores
- * the default.
+ * 0 is raised to 1 and values above 4096 are lowered to 4096).  By default
+ * it follows the kernel the plan is made for: 2 for the single-CTA kernel, 4
+ * for the tensor-memory-Q kernel, 5 for the CTA-pair kernel (about what a
+ * request boundary costs each in pages).  Affects only load balance, never
+ * results.  Process-wide; negative restores the per-kernel defaults.
  */
 MLA_API int mla_set_fixed_overhead(int blocks);
 

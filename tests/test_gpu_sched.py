@@ -90,3 +90,24 @@ def test_fixed_overhead_and_many_requests(fixed):
     assert np.array_equal(parts, ref_parts) and np.array_equal(ns, ref_ns)
     check_plan_invariants(seqlens, parts, ns, int(hdr[3]), fixed)
     check_greedy_fill(seqlens, parts, int(hdr[3]), fixed)
+
+
+def test_default_overhead_follows_the_kernel():
+    """With no overhead set, the plan charges each kernel's measured boundary
+    cost: 4 blocks for tiles the tensor-memory-Q kernel runs (s_q*h_q <= 32),
+    5 for the CTA-pair kernel (>= 128 rows), 2 for the single-CTA kernel."""
+    from decode_attention_paged_gb300 import api
+
+    api.set_fixed_overhead(-1)
+    assert int(device_plan([4096] * 4, 16, 1)[0][5]) == 4
+    assert int(device_plan([4096] * 4, 64, 1)[0][5]) == 2
+    default = api.get_decode_kernel()
+    try:
+        api.set_decode_kernel(api.KERNEL_SINGLE)
+        assert int(device_plan([4096] * 4, 128, 1)[0][5]) == 2
+    finally:
+        api.set_decode_kernel(default)
+    hdr = device_plan([4096] * 4, 128, 1)[0]
+    # one 128-row tile: the CTA-pair kernel (two 64-row tiles if its clusters
+    # cannot be resident and the single-CTA kernel runs instead)
+    assert int(hdr[5]) == (5 if int(hdr[4]) == 1 else 2)
