@@ -23,11 +23,14 @@
 // inside the blocks of a request (more than c units past its start), the
 // part takes blocks up to E and the next part starts there, mid-request;
 // otherwise (E within the c overhead units of request k) not one block of k
-// fits and the next part starts at k's boundary C[k].  So the parts' starts
-// follow one another by a single search each, and every record, piece count
-// and split index follows from those starts with prefix sums and binary
-// searches.  Each reach is at least q past the previous one and the first is
-// q + c, so the parts hold all the work.
+// fits and the next part starts at k's boundary C[k].  Each reach is at
+// least q past the previous one and the first is q + c, so the parts hold
+// all the work.  Reaches that fall inside blocks just add q, so the warp
+// tests 32 consecutive reaches at once (a binary search per lane) and moves
+// to the first that falls into overhead units.  A request's pieces are one
+// plus the cuts inside its blocks; numbered in part order they are numbered
+// request by request, so a part's first piece index is a prefix sum over
+// parts.
 #include "mla_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -37,12 +40,12 @@ __device__ __forceinline__ int64_t blocks_of(int32_t L) {
     return L > 0 ? (static_cast<int64_t>(L) + kPage - 1) / kPage : 0;
 }
 
-// Requests and parts the warp can plan: two int32 arrays of batch + 1 entries
-// and one of parts + 1 live in shared memory (opt-in size).
+// Requests and parts the warp can plan: three int32 arrays of about batch
+// entries and two of parts + 1 live in shared memory (opt-in size).
 constexpr int kSchedMaxBatch = 16384;
 constexpr int kSchedMaxParts = 1024;
 constexpr size_t sched_smem_bytes(int batch, int parts) {
-    return sizeof(int32_t) * (2 * (static_cast<size_t>(batch) + 1) + static_cast<size_t>(parts) + 1);
+    return sizeof(int32_t) * (3 * (static_cast<size_t>(batch) + 1) + 2 * (static_cast<size_t>(parts) + 1));
 }
 
 __device__ __forceinline__ int warp_inclusive_scan(int v) {
@@ -74,8 +77,10 @@ __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ s
     pdl_launch_dependents();
     extern __shared__ int32_t s_buf[];
     int32_t* C = s_buf;                  // C[i]: first cost unit of request i; C[batch] = total
-    int32_t* S = s_buf + batch + 1;      // S[i]: index of request i's first piece; S[batch] = pieces
-    int32_t* X = s_buf + 2 * batch + 2;  // X[p]: first cost unit of part p; X[num_parts] = total
+    int32_t* S = C + batch + 1;          // S[i]: index of request i's first piece; S[batch] = pieces
+    int32_t* PC = S + batch + 1;         // PC[i]: pieces of request i
+    int32_t* X = PC + batch + 1;         // X[p]: first cost unit of part p; total past the last
+    int32_t* K = X + num_parts + 1;      // K[p]: request holding X[p]; batch at the end
     const int lane = threadIdx.x;
     const int c = fixed;
     const int64_t cap_blocks = (1 << 30) / batch - c;
@@ -91,59 +96,75 @@ __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ s
         const int64_t nb = blocks_of(L) < cap_blocks ? blocks_of(L) : cap_blocks;
         const int v = i < batch ? static_cast<int>(nb) + c : 0;
         const int incl = warp_inclusive_scan(v);
-        if (i < batch) C[i + 1] = carry + incl;
+        if (i < batch) {
+            C[i + 1] = carry + incl;
+            PC[i] = 1;
+        }
         carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) C[0] = 0;
+    if (lane == 0) {
+        C[0] = 0;
+        X[0] = 0;
+        K[0] = 0;
+    }
     __syncwarp();
     const int total = C[batch];
     const int q = (total + num_parts - 1) / num_parts;
+    auto nblk = [&](int i) { return C[i + 1] - C[i] - c; };
 
-    // 2. The parts' starts, one after another.  k: the request holding the
-    // current start; the next request holding a reach is found 32 requests
-    // at a time (C increases, so the lanes with C[k + 1 + lane] <= E form a
-    // prefix of the warp).
+    // 2. The parts' starts, 32 reaches per round.  Part p + m reaches
+    // E + m q as long as parts p .. p + m - 1 all end inside blocks.
     {
-        int x = 0, k = 0;
-        bool boundary = true;
         int p = 0;
-        for (; p < num_parts && x < total; ++p) {
-            if (lane == 0) X[p] = x;
-            const int E = x + q + (boundary ? c : 0);
-            if (E >= total) {
-                x = total;
+        int64_t E = static_cast<int64_t>(q) + c;  // part 0 starts at request 0's boundary
+        for (;;) {
+            const int64_t Em = E + static_cast<int64_t>(lane) * q;
+            const bool live = p + lane < num_parts && Em < total;
+            int km = 0;
+            bool snap = false;
+            if (live) {
+                km = last_le(C, batch, static_cast<int>(Em));
+                snap = Em - C[km] <= c;
+            }
+            const unsigned ev = __ballot_sync(0xffffffffu, snap || !live);
+            const int f = ev ? __ffs(ev) - 1 : 32;
+            if (lane < f) {  // part p + lane ends inside request km's blocks
+                X[p + lane + 1] = static_cast<int>(Em);
+                K[p + lane + 1] = km;
+                atomicAdd(&PC[km], 1);
+            }
+            if (f == 32) {
+                p += 32;
+                E += static_cast<int64_t>(32) * q;
                 continue;
             }
-            for (;;) {
-                const int j = k + 1 + lane;
-                const unsigned ok = __ballot_sync(0xffffffffu, j < batch && C[j] <= E);
-                const int n_ok = __popc(ok);
-                k += n_ok;
-                if (n_ok < 32) break;
+            const int kf = __shfl_sync(0xffffffffu, km, f);
+            const bool snapped = __shfl_sync(0xffffffffu, snap ? 1 : 0, f) != 0;
+            if (snapped) {  // part p + f closes at request kf's boundary
+                const int xs = C[kf];
+                if (lane == 0) {
+                    X[p + f + 1] = xs;
+                    K[p + f + 1] = kf;
+                }
+                p += f + 1;
+                E = static_cast<int64_t>(xs) + q + c;
+                continue;
             }
-            if (E - C[k] <= c) {
-                x = C[k];
-                boundary = true;
-            } else {
-                x = E;
-                boundary = false;
+            // Part p + f (if it exists) takes the rest; later parts are empty.
+            for (int r = p + f + 1 + lane; r <= num_parts; r += 32) {
+                X[r] = total;
+                K[r] = batch;
             }
+            break;
         }
-        for (int r = p + lane; r <= num_parts; r += 32) X[r] = total;
     }
     __syncwarp();
 
-    // 3. Pieces per request: the parts holding its first and last block
-    // units (a request without blocks: its first overhead unit).
-    auto nblk = [&](int i) { return C[i + 1] - C[i] - c; };
-    auto part_of = [&](int pos) { return last_le(X, num_parts, pos); };
-    auto first_part = [&](int i) { return part_of(nblk(i) > 0 ? C[i] + c : C[i]); };
+    // 3. num_splits: prefix sums of the pieces per request.
     carry = 0;
     for (int base = 0; base < batch; base += 32) {
         const int i = base + lane;
-        int pc = 0;
-        if (i < batch) pc = nblk(i) > 0 ? part_of(C[i + 1] - 1) - first_part(i) + 1 : 1;
-        const int incl = warp_inclusive_scan(pc);
+        const int incl = warp_inclusive_scan(i < batch ? PC[i] : 0);
         if (i < batch) S[i + 1] = carry + incl;
         carry += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -151,24 +172,41 @@ __global__ void __launch_bounds__(32) sched_kernel(const int32_t* __restrict__ s
     __syncwarp();
     const int pieces_total = S[batch];
 
-    // 4. One record per part: the requests holding its first and last units.
+    // 4. One record per part: first and last requests from the starts of the
+    // part and of the next one, first piece index by a prefix sum over parts.
     int4* rec_out = reinterpret_cast<int4*>(meta + kMetaHeader);
-    for (int p = lane; p < num_parts; p += 32) {
-        const int a = X[p], e = X[p + 1];
-        if (a >= e) {
+    carry = 0;
+    for (int base = 0; base < num_parts; base += 32) {
+        const int p = base + lane;
+        int bq = 0, er = -1, b0 = 0, b1 = 0;
+        const bool used = p < num_parts && X[p] < X[p + 1];
+        if (used) {
+            const int a = X[p], e = X[p + 1];
+            bq = K[p];
+            b0 = a > C[bq] ? a - C[bq] - c : 0;
+            const int kn = K[p + 1];
+            if (kn < batch && e > C[kn]) {  // the next part continues request kn
+                er = kn;
+                b1 = e - C[kn] - c;
+            } else {
+                er = kn - 1;
+                b1 = nblk(er);
+            }
+        }
+        const int np = used ? er - bq + 1 : 0;
+        const int incl = warp_inclusive_scan(np);
+        const int first_piece = carry + incl - np;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        if (p >= num_parts) continue;
+        if (!used) {
             rec_out[2 * p] = make_int4(batch, batch - 1, 0, 0);
             rec_out[2 * p + 1] = make_int4(pieces_total, 0, 0, 0);
             continue;
         }
-        const int bq = last_le(C, batch, a);
-        const int er = last_le(C, batch, e - 1);
-        const int b0 = a > C[bq] ? a - C[bq] - c : 0;
-        const int b1 = e - C[er] - c > 0 ? e - C[er] - c : 0;
-        const int begin_split = S[bq] + (p - first_part(bq));
         const int first_split = (S[bq + 1] - S[bq]) > 1;
         const int last_split = (S[er + 1] - S[er]) > 1;
         rec_out[2 * p] = make_int4(bq, er, b0, b1);
-        rec_out[2 * p + 1] = make_int4(begin_split, first_split, last_split, 0);
+        rec_out[2 * p + 1] = make_int4(first_piece, first_split, last_split, 0);
     }
     for (int i = lane; i <= batch; i += 32) num_splits[i] = S[i];
     if (lane == 0) {
