@@ -39,6 +39,9 @@ SIGNATURES = {
     "mla_workspace_size": (_I, [_I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "mla_decode_fwd": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _F,
                             _I, _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P, _P]),
+    "mla_decode_fwd_dims": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I, _I,
+                                 _I, _I, _I, _F, _I, _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P,
+                                 _P]),
     "mla_decode_splitkv": (_I, [_P, _I64, _P, _I64, _I64, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I,
                                 _F, _I, _P, _P, _P, _SZ, _P, _I64, _I64, _I64, _P, _P]),
     "mla_decode_combine": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _P, _I64, _I64, _I64, _P, _P]),

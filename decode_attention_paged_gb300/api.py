@@ -138,6 +138,46 @@ def mla_decode_fwd(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Te
                       num_splits, workspace, out, lse, stream).fwd()
 
 
+def mla_decode_fwd_dims(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
+                        cache_seqlens: torch.Tensor, softmax_scale: float, causal: bool,
+                        meta: torch.Tensor, num_splits: torch.Tensor, head_dim_v: int,
+                        workspace: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None):
+    """Other head sizes: q [b, s_q, h_q, d] over k_cache [pages, 64, 1, d],
+    V the first head_dim_v dims of each cache row; returns out
+    [b, s_q, h_q, head_dim_v] bf16 and lse [b, h_q, s_q] fp32
+    (mla_decode_fwd_dims in include/mla_decode.h: d and head_dim_v multiples
+    of 64, head_dim_v <= min(d, 512), d <= 576)."""
+    assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
+    assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+    assert meta.dtype == torch.int32 and num_splits.dtype == torch.int32
+    b, s_q, h_q, d = q.shape
+    assert q.stride(3) == 1 and q.stride(2) == d and q.stride(1) == h_q * d, \
+        "q rows must be packed: [b][s_q][h_q][d] with the (s_q, h_q) rows contiguous"
+    num_pages, page, h_kv, dk = k_cache.shape
+    assert dk == d and k_cache.stride(3) == 1 and block_table.stride(1) == 1
+    assert block_table.dim() == 2 and block_table.shape[0] == b
+    for t in (k_cache, block_table, cache_seqlens, meta, num_splits):
+        assert t.device == q.device, "every tensor must be on q's device"
+    dev = q.device
+    cache_seqlens = cache_seqlens.contiguous()
+    with torch.cuda.device(dev):
+        out = torch.empty(b, s_q, h_q, head_dim_v, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(b, h_q, s_q, dtype=torch.float32, device=dev)
+        if workspace is None:
+            workspace = torch.empty(workspace_size(b, h_q, s_q, h_kv), dtype=torch.uint8,
+                                    device=dev)
+        st = _lib.load().mla_decode_fwd_dims(
+            _ptr(q), q.stride(0), _ptr(k_cache), k_cache.stride(0), k_cache.stride(1), num_pages,
+            page, _ptr(block_table), block_table.stride(0), block_table.shape[1],
+            _ptr(cache_seqlens), b, s_q, h_q, h_kv, d, int(head_dim_v), float(softmax_scale),
+            int(bool(causal)), _ptr(meta), _ptr(num_splits), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(out), out.stride(0),
+            out.stride(1), out.stride(2), _ptr(lse), _stream_ptr(stream))
+        _lib.check(st, "mla_decode_fwd_dims")
+    return out, lse
+
+
 def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
                            cache_seqlens: torch.Tensor, softmax_scale: float, causal: bool,
                            meta: torch.Tensor, num_splits: torch.Tensor, out: torch.Tensor,
@@ -350,9 +390,12 @@ def get_decode_kernel() -> int:
 
 def flash_mla_with_kvcache(q, k_cache, block_table, cache_seqlens, head_dim_v, meta, num_splits,
                            softmax_scale=None, causal=False):
-    """The pages' call shape (flash_mla_with_kvcache) mapped onto mla_decode_fwd."""
-    assert head_dim_v == D_V
+    """The pages' call shape (flash_mla_with_kvcache) mapped onto mla_decode_fwd
+    (or mla_decode_fwd_dims for head sizes other than 576 / 512)."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
+    if q.shape[-1] != D_QK or head_dim_v != D_V:
+        return mla_decode_fwd_dims(q, k_cache, block_table, cache_seqlens, softmax_scale, causal,
+                                   meta, num_splits, head_dim_v)
     return mla_decode_fwd(q, k_cache, block_table, cache_seqlens, softmax_scale, causal, meta,
                           num_splits)

@@ -307,7 +307,7 @@ namespace {
 int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
                  int kvh, int grp, void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
-                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream);
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream, int dv = kDv);
 
 int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int s_q, int h_q, int h_kv, void* out_dev,
@@ -335,7 +335,7 @@ int combine_only(const void* meta_dev, const int32_t* num_splits_dev, void* work
 int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* workspace_dev,
                  size_t workspace_bytes, int batch, int R, int parts, int s_q, int h_q, int fold,
                  int kvh, int grp, void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
-                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream, int dv) {
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(batch, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -358,6 +358,7 @@ int combine_core(const void* meta_dev, const int32_t* num_splits_dev, void* work
     c.fold = fold;
     c.kvh = kvh;
     c.grp = grp;
+    c.dv = dv;
     cudaError_t e = launch_combine(c, reinterpret_cast<cudaStream_t>(stream), /*pdl=*/true);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -369,17 +370,24 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
                  float softmax_scale, int causal, const void* meta_dev,
                  const int32_t* num_splits_dev, void* workspace_dev, size_t workspace_bytes,
                  void* out_dev, int64_t out_batch_stride, int64_t out_s_stride,
-                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream) {
+                 int64_t out_h_stride, float* lse_dev, mla_stream_t stream, int d_qk = kDqk,
+                 int d_v = kDv) {
     int st = check_shape(batch, h_q, s_q, h_kv);
     if (st) return st;
     if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    // Other head sizes: 64-dim chunks, V the first d_v dims of each K row, one
+    // cache head, on the single-CTA kernel.
+    const bool general = d_qk != kDqk || d_v != kDv;
+    if (general && (d_qk % 64 || d_qk < 64 || d_qk > kDqk || d_v % 64 || d_v < 64 ||
+                    d_v > kDv || d_v > d_qk || h_kv != 1))
+        return MLA_ERR_UNSUPPORTED;
     if (!q_dev || !k_cache_dev || !block_table_dev || !cache_seqlens_dev || !meta_dev ||
         !num_splits_dev || !out_dev || !lse_dev)
         return MLA_ERR_INVALID_ARGUMENT;
     if (num_pages < 1 || max_blocks_per_seq < 1 || bt_batch_stride < max_blocks_per_seq ||
-        q_batch_stride < static_cast<int64_t>(s_q) * h_q * kDqk ||
-        k_token_stride < static_cast<int64_t>(h_kv) * kDqk ||
-        k_page_stride < k_token_stride * kPage || out_h_stride < kDv ||
+        q_batch_stride < static_cast<int64_t>(s_q) * h_q * d_qk ||
+        k_token_stride < static_cast<int64_t>(h_kv) * d_qk ||
+        k_page_stride < k_token_stride * kPage || out_h_stride < d_v ||
         out_s_stride < out_h_stride * h_q || out_batch_stride < out_s_stride * s_q ||
         !std::isfinite(softmax_scale) || (causal != 0 && causal != 1))
         return MLA_ERR_INVALID_ARGUMENT;
@@ -393,8 +401,10 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     const int R = g.R;
+    // (The plan's part count is mla_get_metadata's, for whichever kernel it
+    // was made; the single-CTA kernel runs any part count.)
     const int parts = num_parts_of(R, h_kv, d);
-    const int kind = kernel_for(R, h_kv, d);
+    const int kind = general ? MLA_KERNEL_SINGLE : kernel_for(R, h_kv, d);
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(g.nreq, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -404,10 +414,10 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
     if (kind == MLA_KERNEL_DUO) q_box_rows = kTileM;  // each CTA of a pair loads 64 rows
     if (h_kv == 1) {
-        st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
-                       kDqk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
+        st = encode_3d(&q_map, q_dev, d_qk, static_cast<uint64_t>(R), static_cast<uint64_t>(batch),
+                       d_qk * 2, static_cast<uint64_t>(q_batch_stride) * 2, q_box_rows);
         if (st) return st;
-        st = encode_3d(&kv_map, k_cache_dev, kDqk, kPage, static_cast<uint64_t>(num_pages),
+        st = encode_3d(&kv_map, k_cache_dev, d_qk, kPage, static_cast<uint64_t>(num_pages),
                        static_cast<uint64_t>(k_token_stride) * 2,
                        static_cast<uint64_t>(k_page_stride) * 2, kPage);
         if (st) return st;
@@ -465,6 +475,10 @@ int splitkv_only(const void* q_dev, int64_t q_batch_stride, const void* k_cache_
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
     p.kvh = g.kvh;
     p.grp = g.grp;
+    if (general) {
+        p.nc = d_qk / 64;
+        p.nv = d_v / 64;
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = kind == MLA_KERNEL_TQ    ? launch_decode_tq(p, q_map, kv_map, s)
@@ -520,6 +534,30 @@ int mla_decode_fwd(const void* q_dev, int64_t q_batch_stride, const void* k_cach
     return combine_only(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, batch, s_q, h_q,
                         h_kv, out_dev, out_batch_stride, out_s_stride, out_h_stride, lse_dev,
                         stream);
+}
+
+int mla_decode_fwd_dims(const void* q_dev, int64_t q_batch_stride, const void* k_cache_dev,
+                        int64_t k_page_stride, int64_t k_token_stride, int num_pages,
+                        int page_size, const int32_t* block_table_dev, int64_t bt_batch_stride,
+                        int max_blocks_per_seq, const int32_t* cache_seqlens_dev, int batch,
+                        int s_q, int h_q, int h_kv, int d_qk, int d_v, float softmax_scale,
+                        int causal, const void* meta_dev, const int32_t* num_splits_dev,
+                        void* workspace_dev, size_t workspace_bytes, void* out_dev,
+                        int64_t out_batch_stride, int64_t out_s_stride, int64_t out_h_stride,
+                        float* lse_dev, mla_stream_t stream) {
+    int st = splitkv_only(q_dev, q_batch_stride, k_cache_dev, k_page_stride, k_token_stride,
+                          num_pages, page_size, block_table_dev, bt_batch_stride,
+                          max_blocks_per_seq, cache_seqlens_dev, batch, s_q, h_q, h_kv,
+                          softmax_scale, causal, meta_dev, num_splits_dev, workspace_dev,
+                          workspace_bytes, out_dev, out_batch_stride, out_s_stride, out_h_stride,
+                          lse_dev, stream, d_qk, d_v);
+    if (st) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = device_info(&d))) return st;
+    const Geo g = geo_of(batch, h_q, s_q, h_kv);
+    return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, g.nreq, g.R,
+                        num_parts_of(g.R, h_kv, d), s_q, h_q, 0, g.kvh, g.grp, out_dev,
+                        out_batch_stride, out_s_stride, out_h_stride, lse_dev, stream, d_v);
 }
 
 int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,

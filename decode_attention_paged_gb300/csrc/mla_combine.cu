@@ -171,7 +171,74 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineParams p) {
     if (lane == 0) *lse_out = (mx + fast_log2(wsum)) * 0.69314718055994531f;
 }
 
+// Rows of dv != 512 floats (mla_decode_fwd_dims): the same merge, one warp
+// per row, four rows per CTA; lane l owns dims [l nd, l nd + nd), nd = dv / 32
+// (even), read as float2.
+__global__ void __launch_bounds__(128) combine_dims_kernel(CombineParams p) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int req = blockIdx.y, row = blockIdx.x * 4 + warp;
+    pdl_launch_dependents();
+    pdl_wait_primary();
+    if (ld_i(p.meta + kHMagic) != kMetaMagic || ld_i(p.meta + kHBatch) != p.batch ||
+        ld_i(p.meta + kHRows) != p.R || row >= p.R)
+        return;
+    const int first = ld_i(p.num_splits + req);
+    const int n = ld_i(p.num_splits + req + 1) - first;
+    if (n <= 1) return;
+    const int dv = p.dv, nd = dv / 32;
+    const float* lse_base = p.lseaccum + static_cast<int64_t>(first) * p.R + row;
+    float mx = -INFINITY;
+    for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ld_f(lse_base + static_cast<int64_t>(k) * p.R));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const OutMap om =
+        out_map(req, row, p.h_q, p.s_q, p.fold, p.kvh, p.grp, p.out_sb, p.out_ss, p.out_sh);
+    __nv_bfloat16* orow = p.out + om.out_off + lane * nd;
+    if (mx == -INFINITY) {
+        for (int i = 0; i < nd; i += 2) *reinterpret_cast<uint32_t*>(orow + i) = 0u;
+        if (lane == 0) p.lse[om.lse_idx] = -INFINITY;
+        return;
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * dv + lane * nd;
+    for (int k = 0; k < n; ++k) {
+        const float lk = ld_f(lse_base + static_cast<int64_t>(k) * p.R);
+        const float w = (lk == -INFINITY) ? 0.f : fast_exp2(lk - mx);
+        wsum += w;
+        const float* src = o_base + static_cast<int64_t>(k) * p.R * dv;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            if (i < nd) {
+                float2 v;
+                asm volatile("ld.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(src + i));
+                acc[i] += w * v.x;
+                acc[i + 1] += w * v.y;
+            }
+        }
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2)
+        if (i < nd) *reinterpret_cast<uint32_t*>(orow + i) = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+    if (lane == 0) p.lse[om.lse_idx] = (mx + fast_log2(wsum)) * 0.69314718055994531f;
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl) {
+    if (p.dv != 0 && p.dv != kDv) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((p.R + 3) / 4, p.batch, 1);
+        cfg.blockDim = dim3(128, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, combine_dims_kernel, p);
+    }
     // Warps per row from the average number of pieces per request (the plan
     // has at most batch + parts pieces): when requests average eight pieces or
     // more (few long sequences spread over many SM parts) eight warps share

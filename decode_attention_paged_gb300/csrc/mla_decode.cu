@@ -263,7 +263,9 @@ __device__ __forceinline__ void issue_qk_turn(uint64_t dQ, uint64_t bK, uint32_t
 // registers would otherwise raise every launch's register count).
 // kHeads: several cache heads (p.kvh > 1); with one head the request and
 // head arithmetic folds away (measured 5% on the h_q = 128 workloads).
-template <bool kStageP, bool kFp8, bool kHeads>
+// kGen: other head sizes (p.nc, p.nv chunks of 64 dims for d and dv; bf16,
+// one cache head), with the 576 / 512 instantiations left as they are.
+template <bool kStageP, bool kFp8, bool kHeads, bool kGen = false>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap kv_map) {
@@ -272,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mtile = blockIdx.x, part_idx = blockIdx.y;
     const int kvh = kHeads ? p.kvh : 1;     // cache heads
     const int grp = kHeads ? p.grp : p.h_q;  // query heads per cache head
+    const int nc = kGen ? p.nc : kChunks;   // 64-dim chunks of a K / Q row
+    const int nv = kGen ? p.nv : kDv / 64;  // 64-dim chunks of a V row
+    const int dv = 64 * nv;
 
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sKV = smem + kOffKV;
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Sparse decode: the gather warps fill the KV ring; this warp only
         // loads each request's Q tile.
         const uint64_t policy = policy_evict_first();
-        const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
+        const uint32_t q_bytes = nc * p.q_box_rows * 128;
         const bool sparse = p.sparse != 0;
         Cursor ld = cursor_begin<kHeads>(p, part), ahead = ld;
         auto fetch_window = [&](uint32_t slot) {
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->q_full, q_bytes);
                 if (!kHeads) {
-                    for (int c = 0; c < kChunks; ++c)
+                    for (int c = 0; c < nc; ++c)
                         tma_load_3d(&q_map, &bars->q_full, sQ + c * kChunkBytes, 64 * c,
                                     mtile * kTileM, req, policy);
                 } else {
@@ -457,9 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mbar_arrive(&bars->raw_full[st]);
                         }
                     } else {
-                        mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                        mbar_arrive_expect_tx(&bars->kv_full[st], nc * kChunkBytes);
                         if (!kHeads) {
-                            for (int c = 0; c < kChunks; ++c)
+                            for (int c = 0; c < nc; ++c)
                                 tma_load_3d(&kv_map, &bars->kv_full[st], dst + c * kChunkBytes,
                                             64 * c, 0, page, policy);
                         } else {  // map (576, h_kv, 64, pages): this request's cache head
@@ -552,11 +557,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t acc0 = first ? 0u : 1u;
                     // One elected thread issues the burst and commits it.
                     if (elect_one()) {
+                        if (!kGen) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t acc = kk ? 1u : acc0;
-                            mma_ws_ss(tO0, dP + 2 * kk, bV + 128 * kk, idesc_pv, acc);
-                            mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk, idesc_pv, acc);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint32_t acc = kk ? 1u : acc0;
+                                mma_ws_ss(tO0, dP + 2 * kk, bV + 128 * kk, idesc_pv, acc);
+                                mma_ws_ss(tO1, dP + 2 * kk, bV + 4 * kChunkUnits + 128 * kk,
+                                          idesc_pv, acc);
+                            }
+                        } else {
+                            // V chunks in groups of 4, 2 or 1 (N = 256, 128,
+                            // 64): group [cs, cs + n) writes TMEM columns
+                            // 32 cs .. 32 (cs + n) (dims 64 cs + [0, 32 n) in
+                            // lanes 0..63, 64 cs + [32 n, 64 n) in 64..127).
+                            for (int cs = 0; cs < nv;) {
+                                const int n = nv - cs >= 4 ? 4 : (nv - cs >= 2 ? 2 : 1);
+                                const uint32_t idesc_g = idesc_bf16_f32(64, 64 * n, false, true);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ws_ss(tmem + kColO + 32 * cs, dP + 2 * kk,
+                                              bV + cs * kChunkUnits + 128 * kk, idesc_g,
+                                              kk ? 1u : acc0);
+                                cs += n;
+                            }
                         }
                         mma_commit(&bars->pv_done[pv.g & 1]);
                         mma_commit(&bars->kv_empty[pv.g & 1]);
@@ -581,9 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bK = st ? dK1 : dK0;
                     const uint32_t d = st ? tS1 : tS0;
                     if (elect_one()) {
-                        issue_qk_turn<0>(dQ, bK, d);
-                        issue_qk_turn<3>(dQ, bK, d);
-                        issue_qk_turn<6>(dQ, bK, d);
+                        if (!kGen) {
+                            issue_qk_turn<0>(dQ, bK, d);
+                            issue_qk_turn<3>(dQ, bK, d);
+                            issue_qk_turn<6>(dQ, bK, d);
+                        } else {
+                            constexpr uint32_t idesc_qk = idesc_bf16_f32(64, 64, false, false);
+                            for (int c = 0; c < nc; ++c)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ws_ss(d, dQ + c * kChunkUnits + 2 * kk,
+                                              bK + c * kChunkUnits + 2 * kk, idesc_qk,
+                                              (c + kk) ? 1u : 0u);
+                        }
                         mma_commit(&bars->s_full[st]);
                         if (qk.blk == qk.b1 - 1) mma_commit(&bars->q_empty);
                     }
@@ -831,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rescale) {
                     const float a = (need && blk > b0) ? alpha : 1.f;
 #pragma unroll 1
-                    for (int cg = 0; cg < 8; ++cg) {
+                    for (int cg = 0; cg < nv; ++cg) {
                         uint32_t o[32];
                         tmem_ld32(tl + kColO + 32 * cg, o);
                         tmem_ld_wait();
@@ -848,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tail0 = L & (kPage - 1);
                     const int per_chunk = (kPage - tail0) * 8;  // 16-byte units
                     uint8_t* stage = sKV + st * kStageBytes;
-                    for (int i = tid - 64; i < 8 * per_chunk; i += 128) {
+                    for (int i = tid - 64; i < nv * per_chunk; i += 128) {
                         const int c = i / per_chunk, u = i % per_chunk;
                         reinterpret_cast<uint4*>(stage + c * kChunkBytes + tail0 * 128)[u] =
                             make_uint4(0, 0, 0, 0);
@@ -892,14 +925,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       p.out_ss, p.out_sh);
             if (has_blocks) {
 #pragma unroll 1
-                for (int cg = 0; cg < 8; ++cg) {
+                for (int cg = 0; cg < nv; ++cg) {
                     uint32_t o[32];
                     tmem_ld32(tl + kColO + 32 * cg, o);
                     tmem_ld_wait();
-                    const int dv0 = 256 * (cg >> 2) + 128 * half + 32 * (cg & 3);
+                    // This thread's 32 dims of TMEM columns 32 cg .. 32 cg + 31
+                    // (the PV groups of the MMA issuer: 4, 4 chunks for 512).
+                    int dv0 = 256 * (cg >> 2) + 128 * half + 32 * (cg & 3);
+                    if (kGen) {
+                        for (int cs = 0;;) {
+                            const int n = nv - cs >= 4 ? 4 : (nv - cs >= 2 ? 2 : 1);
+                            if (cg < cs + n) {
+                                dv0 = 64 * cs + 32 * n * half + 32 * (cg - cs);
+                                break;
+                            }
+                            cs += n;
+                        }
+                    }
                     if (!row_valid) continue;
                     if (split) {
-                        float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
+                        float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * dv + dv0);
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv,
@@ -924,11 +969,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++n_items;
             } else if (row_valid) {
                 if (split) {
-                    float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv);
-                    for (int v = 0; v < 64; ++v) dst[v * 2 + half] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * dv);
+                    for (int v = 0; v < dv / 8; ++v) dst[v * 2 + half] = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + om.out_off);
-                    for (int v = 0; v < 32; ++v) dst[v * 2 + half] = make_uint4(0, 0, 0, 0);
+                    for (int v = 0; v < dv / 16; ++v) dst[v * 2 + half] = make_uint4(0, 0, 0, 0);
                 }
             }
             if (row_valid && half == 0) {
@@ -950,20 +995,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, cudaStream_t stream) {
     // The instantiations a launch can pick: P placement x {bf16, FP8, bf16
-    // with several cache heads} (FP8 has one cache head).
+    // with several cache heads, bf16 with other head sizes} (FP8 and other
+    // head sizes have one cache head).
     using Kernel = void (*)(DecodeParams, CUtensorMap, CUtensorMap);
-    static const Kernel kernels[2][3] = {
+    static const Kernel kernels[2][4] = {
         {decode_kernel<false, false, false>, decode_kernel<false, true, false>,
-         decode_kernel<false, false, true>},
+         decode_kernel<false, false, true>, decode_kernel<false, false, false, true>},
         {decode_kernel<true, false, false>, decode_kernel<true, true, false>,
-         decode_kernel<true, false, true>}};
+         decode_kernel<true, false, true>, decode_kernel<true, false, false, true>}};
     static int configured_mask = 0;  // per-device "smem attribute set" bits (first 31 devices)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(configured_mask & (1 << dev))) {
         for (int sp = 0; sp < 2; ++sp)
-            for (int m = 0; m < 3; ++m) {
+            for (int m = 0; m < 4; ++m) {
                 e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernels[sp][m]),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sp ? kSmemBytes : kSmemBytesP));
@@ -981,7 +1027,9 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& q_map,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int mode = p.fp8 ? 1 : (p.kvh > 1 ? 2 : 0);
+    // (nc = nv = 0: the 576 / 512 sizes every other call uses.)
+    const bool general = (p.nc != 0 && p.nc != kChunks) || (p.nv != 0 && p.nv != kDv / 64);
+    const int mode = p.fp8 ? 1 : (p.kvh > 1 ? 2 : (general ? 3 : 0));
     return cudaLaunchKernelEx(&cfg, kernels[p.stage_p ? 1 : 0][mode], p, q_map, kv_map);
 }
 

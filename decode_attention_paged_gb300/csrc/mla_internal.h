@@ -88,6 +88,10 @@ struct DecodeParams {
     // decode_kernel only: 1 = P of each page in that page's RoPE chunk (the
     // softmax may run a page ahead of PV), 0 = one P buffer.
     int stage_p;
+    // decode_kernel's head-size instantiation only: K / Q rows of nc 64-dim
+    // chunks (d = 64 nc <= 576), V their first nv chunks (dv = 64 nv <= 512);
+    // the partials in oaccum are rows of dv floats.
+    int nc, nv;
 };
 
 // Output address of (kernel request r, row) for every layout: dense
@@ -126,6 +130,7 @@ struct CombineParams {
     int num_parts;  // SM parts of the plan (bounds the pieces: batch + num_parts)
     int fold;      // as DecodeParams::fold
     int kvh, grp;  // as DecodeParams::kvh, grp
+    int dv;        // partial row length (512, or a head-size call's dv)
 };
 
 // Host launchers (return a cudaError_t).

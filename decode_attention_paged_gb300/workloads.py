@@ -74,9 +74,10 @@ def _randn_bf16(shape, seed: int) -> torch.Tensor:
 
 def make(name: str, b: int, s_q: int, h_q: int, seqlens: Sequence[int], num_pages: int,
          max_blocks: Optional[int] = None, causal: bool = False, seed_offset: int = 0,
-         block_table: Optional[torch.Tensor] = None, scale: float = SCALE) -> Workload:
+         block_table: Optional[torch.Tensor] = None, scale: float = SCALE,
+         d: int = D_QK) -> Workload:
     """Generic workload: block_table = randperm(num_pages)[:b*max_blocks].view(b, max_blocks)
-    unless given."""
+    unless given; q and cache rows of d dims (576 unless given)."""
     seqlens = torch.tensor(list(seqlens), dtype=torch.int32)
     assert seqlens.numel() == b
     need = max(1, max((int(x) + PAGE - 1) // PAGE for x in seqlens.tolist()) if b else 1)
@@ -87,8 +88,8 @@ def make(name: str, b: int, s_q: int, h_q: int, seqlens: Sequence[int], num_page
         assert num_pages >= b * max_blocks, "page pool too small for a permutation"
         perm = torch.randperm(num_pages, generator=_gen(3 + seed_offset)).to(torch.int32)
         block_table = perm[: b * max_blocks].view(b, max_blocks).contiguous()
-    q = _randn_bf16((b, s_q, h_q, D_QK), 1 + seed_offset)
-    k_cache = _randn_bf16((num_pages, PAGE, 1, D_QK), 2 + seed_offset)
+    q = _randn_bf16((b, s_q, h_q, d), 1 + seed_offset)
+    k_cache = _randn_bf16((num_pages, PAGE, 1, d), 2 + seed_offset)
     return Workload(name, q, k_cache, block_table.to(torch.int32), seqlens, scale, causal)
 
 
@@ -136,11 +137,13 @@ CONFIG_ORDER = ["tiny", "memory_bound", "compute_bound", "mtp", "long_ragged"]
 
 
 def random_case(seed: int, b: int, s_q: int, h_q: int, seqlens: Sequence[int], causal: bool,
-                extra_pages: int = 3) -> Workload:
-    """A small random case whose pool has a few pages no sequence references."""
+                extra_pages: int = 3, d: int = D_QK) -> Workload:
+    """A small random case whose pool has a few pages no sequence references
+    (rows of d dims; softmax_scale d^-0.5)."""
     need = max(1, max((int(x) + PAGE - 1) // PAGE for x in seqlens))
     return make(f"random seed{seed}", b, s_q, h_q, seqlens, b * need + extra_pages, need,
-                causal=causal, seed_offset=10 * seed)
+                causal=causal, seed_offset=10 * seed, d=d,
+                scale=SCALE if d == D_QK else d ** -0.5)
 
 
 def flops(seqlens: Sequence[int], s_q: int, h_q: int, causal: bool) -> int:

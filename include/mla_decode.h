@@ -35,7 +35,8 @@
  *     block-table row, metadata built for another shape, a pipeline wait that
  *     exceeded its time budget) are recorded in a per-device error word and
  *     reported by mla_last_device_error().
- * Supported: bf16 q / k_cache / out, fp32 lse, d_qk = 576, d_v = 512, page
+ * Supported: bf16 q / k_cache / out, fp32 lse, d_qk = 576, d_v = 512 (other
+ * sizes through mla_decode_fwd_dims), page
  * size 64, batch * h_kv <= 16384, GPUs of compute capability 10.3 (GB300);
  * other shapes return MLA_ERR_UNSUPPORTED.
  *
@@ -180,6 +181,32 @@ MLA_API int mla_decode_fwd(const void *q_dev, int64_t q_batch_stride, const void
                    const int32_t *num_splits_dev, void *workspace_dev, size_t workspace_bytes,
                    void *out_dev, int64_t out_batch_stride, int64_t out_s_stride,
                    int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
+
+/*
+ * mla_decode_fwd_dims -- mla_decode_fwd for other head sizes: q rows and
+ * cache rows of d_qk dims, out rows of d_v dims, V again the first d_v dims
+ * of each cache row.  The pages' decode has d_qk = 576, d_v = 512 ("[DeepSeek-3]
+ * FlashMLA", sec. 3; the reference tests' configuration in "FlashMLA 新内核深度
+ * 解析", "如何在仓库中验证与复现"); this call takes any d_qk and d_v that are
+ * multiples of 64 with 64 <= d_v <= d_qk <= 576 and d_v <= 512, for one cache
+ * head (h_kv = 1), bf16, on the single-CTA kernel.  Other sizes return
+ * MLA_ERR_UNSUPPORTED.  Strides and layouts as mla_decode_fwd with 576 read
+ * as d_qk and 512 as d_v: q [batch][s_q][h_q][d_qk], k_cache
+ * [num_pages][64][1][d_qk] (k_token_stride >= d_qk), out
+ * [batch][s_q][h_q][d_v] (out_h_stride >= d_v).  The plan and the workspace
+ * are those of mla_get_metadata / mla_workspace_size for the same batch,
+ * h_q, s_q and h_kv.  d_qk = 576, d_v = 512 is exactly mla_decode_fwd.
+ */
+MLA_API int mla_decode_fwd_dims(const void *q_dev, int64_t q_batch_stride, const void *k_cache_dev,
+                                int64_t k_page_stride, int64_t k_token_stride, int num_pages,
+                                int page_size, const int32_t *block_table_dev,
+                                int64_t bt_batch_stride, int max_blocks_per_seq,
+                                const int32_t *cache_seqlens_dev, int batch, int s_q, int h_q,
+                                int h_kv, int d_qk, int d_v, float softmax_scale, int causal,
+                                const void *meta_dev, const int32_t *num_splits_dev,
+                                void *workspace_dev, size_t workspace_bytes, void *out_dev,
+                                int64_t out_batch_stride, int64_t out_s_stride,
+                                int64_t out_h_stride, float *lse_dev, mla_stream_t stream);
 
 /*
  * mla_decode_splitkv / mla_decode_combine -- the two kernels mla_decode_fwd

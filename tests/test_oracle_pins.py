@@ -273,3 +273,25 @@ def test_full_problem_row_subset_matches():
     for k, (i, rho) in enumerate(units):
         s, h = divmod(int(rho), 4)
         assert np.array_equal(o[k], out[i, s, h]) and l[k] == lse[i, h, s]
+
+
+@pytest.mark.parametrize("d,dv", [(192, 128), (64, 64), (320, 192), (576, 448)])
+def test_other_head_sizes_match_torch_sdpa(d, dv):
+    """Head sizes other than 576 / 512 (V = the first dv dims of each cache
+    row): the definition again reduces to fp64 scaled_dot_product_attention
+    per request, causal rows included."""
+    w = W.random_case(11, 3, 2, 8, [130, 64, 5], True, d=d)
+    out, lse = oracle.mla_decode(_problem(w), dv=dv, nthreads=2)
+    for i in range(w.b):
+        kv = _gather(w, i)
+        L = kv.shape[0]
+        q = w.q[i].double().reshape(2 * 8, -1)
+        s_idx = torch.arange(2 * 8) // 8
+        mask = torch.arange(L)[None, :] <= (L - 2 + s_idx)[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None], kv[None], kv[None, :, :dv], attn_mask=mask[None], scale=w.softmax_scale)[0]
+        scores = ((q @ kv.T) * w.softmax_scale).masked_fill(~mask, float("-inf"))
+        got = torch.from_numpy(out[i].reshape(2 * 8, dv))
+        assert torch.allclose(got, ref, atol=1e-12, rtol=1e-10)
+        assert torch.allclose(torch.from_numpy(lse[i].T.reshape(-1)), torch.logsumexp(scores, -1),
+                              atol=1e-10, rtol=0)
