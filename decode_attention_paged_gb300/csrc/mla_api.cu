@@ -112,9 +112,20 @@ int num_parts_of(int R, int h_kv, const DeviceInfo* d) {
     return parts > 0 ? parts : 1;
 }
 
-// Sparse decode always runs on the single-CTA kernel.
 int num_parts_single(int R, const DeviceInfo* d) {
     const int parts = d->sms / n_mtiles_of(R);
+    return parts > 0 ? parts : 1;
+}
+
+// Sparse decode: the CTA pair where the dense choice would take it (lists of
+// at least 128 query rows), else the single-CTA kernel (the other kernel
+// does no row gather).
+int sparse_kind(int R, const DeviceInfo* d) {
+    return kernel_for(R, 1, d) == MLA_KERNEL_DUO ? MLA_KERNEL_DUO : MLA_KERNEL_SINGLE;
+}
+int num_parts_sparse(int R, const DeviceInfo* d) {
+    if (sparse_kind(R, d) != MLA_KERNEL_DUO) return num_parts_single(R, d);
+    const int parts = d->duo_clusters / tiles_of(R, MLA_KERNEL_DUO);
     return parts > 0 ? parts : 1;
 }
 
@@ -566,7 +577,7 @@ int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* meta
     if (st) return st;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    const int parts = num_parts_single(h_q, d);
+    const int parts = num_parts_sparse(h_q, d);
     if (meta_bytes)
         *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
     if (num_splits_bytes)
@@ -584,8 +595,9 @@ int mla_get_metadata_sparse(int topk, int batch, int h_q, int s_q, int h_kv, voi
         return MLA_ERR_BAD_ALIGNMENT;
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
-    cudaError_t e = launch_sched(nullptr, 1, topk, batch * s_q, h_q, num_parts_single(h_q, d),
-                                 n_mtiles_of(h_q), fixed_overhead_for(MLA_KERNEL_SINGLE),
+    const int kind = sparse_kind(h_q, d);
+    cudaError_t e = launch_sched(nullptr, 1, topk, batch * s_q, h_q, num_parts_sparse(h_q, d),
+                                 tiles_of(h_q, kind), fixed_overhead_for(kind),
                                  static_cast<int32_t*>(meta_dev), num_splits_dev,
                                  reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -598,7 +610,7 @@ int mla_workspace_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* byt
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     size_t ob = 0;
-    workspace_layout(batch * s_q, h_q, num_parts_single(h_q, d), &ob, bytes);
+    workspace_layout(batch * s_q, h_q, num_parts_sparse(h_q, d), &ob, bytes);
     return MLA_OK;
 }
 
@@ -636,13 +648,15 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     DeviceInfo* d = nullptr;
     if ((st = device_info(&d))) return st;
     const int nreq = batch * s_q, R = h_q;
-    const int parts = num_parts_single(R, d);
+    const int kind = sparse_kind(R, d);
+    const int parts = num_parts_sparse(R, d);
     size_t o_bytes = 0, ws_need = 0;
     workspace_layout(nreq, R, parts, &o_bytes, &ws_need);
     if (!workspace_dev || workspace_bytes < ws_need) return MLA_ERR_WORKSPACE_TOO_SMALL;
     if (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) return MLA_ERR_BAD_ALIGNMENT;
 
     CUtensorMap q_map, kv_map;
+    // (Each CTA of a pair loads 64 query rows.)
     const uint32_t q_box_rows = R < kTileM ? static_cast<uint32_t>(R) : kTileM;
     const int64_t q_req_stride = s_q == 1 ? q_batch_stride : q_tok;
     st = encode_3d(&q_map, q_dev, kDqk, static_cast<uint64_t>(R), static_cast<uint64_t>(nreq),
@@ -670,7 +684,7 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     p.s_q = s_q;
     p.h_q = h_q;
     p.R = R;
-    p.n_mtiles = n_mtiles_of(R);
+    p.n_mtiles = tiles_of(R, kind);
     p.num_parts = parts;
     p.q_box_rows = static_cast<int>(q_box_rows);
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -687,7 +701,10 @@ int mla_decode_sparse_fwd(const void* q_dev, int64_t q_batch_stride, const void*
     p.stage_p = p.n_mtiles == 1 ? 1 : 0;
     p.kvh = 1;
     p.grp = h_q;
-    cudaError_t e = launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        kind == MLA_KERNEL_DUO
+            ? launch_decode_duo(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream))
+            : launch_decode(p, q_map, kv_map, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     return combine_core(meta_dev, num_splits_dev, workspace_dev, workspace_bytes, nreq, R, parts,
                         s_q, h_q, s_q, 1, h_q, out_dev, out_batch_stride, out_s_stride,

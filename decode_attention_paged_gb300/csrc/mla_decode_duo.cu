@@ -68,6 +68,8 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPvWarp = 10;  // the leader's PV issuer (idle in the peer)
 constexpr int kThreads = 352;
+constexpr int kGatherWarp0 = 11;      // sparse decode: warps 11..14 gather rows
+constexpr int kThreadsSparse = 480;
 constexpr int kPairRows = 128;  // query rows of one CTA pair
 constexpr int kCtaRows = 64;    // rows of one CTA
 constexpr int kStages = 5;
@@ -127,9 +129,10 @@ struct Part {
 
 __device__ __forceinline__ int blocks_of(int L) { return L > 0 ? (L + kPage - 1) / kPage : 0; }
 
+template <bool kSparse>
 __device__ __forceinline__ void item_range(const DecodeParams& p, const Part& part, int req,
                                            int& L, int& nb, int& b0, int& b1) {
-    L = p.seqlens[req];
+    L = kSparse ? p.topk : p.seqlens[req];
     if (L < 0) L = 0;
     nb = blocks_of(L);
     if (nb > p.max_blocks) nb = p.max_blocks;  // reported as MLA_ERR_SEQ_TOO_LONG
@@ -151,10 +154,11 @@ struct Cursor {
     bool valid;
     __device__ __forceinline__ uint32_t ring() const { return g + 2 * item + 2; }
 };
+template <bool kSparse>
 __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& part, Cursor& c,
                                             int req) {
     for (; req <= part.end_req; ++req) {
-        item_range(p, part, req, c.L, c.nb, c.b0, c.b1);
+        item_range<kSparse>(p, part, req, c.L, c.nb, c.b0, c.b1);
         if (c.b1 > c.b0) {
             c.req = req;
             c.blk = c.b0;
@@ -164,18 +168,20 @@ __device__ __forceinline__ void cursor_seek(const DecodeParams& p, const Part& p
     }
     c.valid = false;
 }
+template <bool kSparse>
 __device__ __forceinline__ Cursor cursor_begin(const DecodeParams& p, const Part& part) {
     Cursor c;
     c.g = 0;
     c.item = 0;
-    cursor_seek(p, part, c, part.begin_req);
+    cursor_seek<kSparse>(p, part, c, part.begin_req);
     return c;
 }
+template <bool kSparse>
 __device__ __forceinline__ void cursor_next(const DecodeParams& p, const Part& part, Cursor& c) {
     ++c.g;
     if (++c.blk < c.b1) return;
     ++c.item;
-    cursor_seek(p, part, c, c.req + 1);
+    cursor_seek<kSparse>(p, part, c, c.req + 1);
 }
 
 // Warp-uniform bounded wait (lane 0 polls; cluster-scope acquire, since some
@@ -243,7 +249,8 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kSparse>
+__global__ void __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
     decode_duo_kernel(const __grid_constant__ DecodeParams p,
                       const __grid_constant__ CUtensorMap q_map,
                       const __grid_constant__ CUtensorMap kv_map) {
@@ -260,13 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     Barriers* bars = reinterpret_cast<Barriers*>(smem + kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    // Sparse decode: key_mask[stage] has bit t set when stage row t holds a
+    // key (16 bits from each gather warp, written before its kv_full arrival).
+    volatile uint64_t* key_mask = reinterpret_cast<volatile uint64_t*>(smem + kOffMisc + 16);
+    volatile uint16_t* key_mask16 = reinterpret_cast<volatile uint16_t*>(smem + kOffMisc + 16);
     WaitCtx wc{abort_flag, p.error_word, p.budget_ns};
 
     // ------------------------------------------------------------ prologue
     if (tid == 0) {
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_full[s], kSparse ? 4 : 1);
             mbar_init(&bars->kv_peer[s], 1);
             mbar_init(&bars->kv_empty[s], 1);
         }
@@ -322,14 +333,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         part.begin_req = 0;
         part.end_req = -1;
     }
-    if (tid == 0 && leader) {
+    if (tid == 0 && leader && !kSparse) {
         for (int req = part.begin_req; req <= part.end_req; ++req) {
             const int L = p.seqlens[req];
             if (L > 0 && blocks_of(L) > p.max_blocks) raise_error(wc, MLA_ERR_SEQ_TOO_LONG);
         }
     }
 
-    if (warp == kProducerWarp) {
+    if (kSparse && warp >= kGatherWarp0) {
+        // ------------------------------------------- sparse: row gather
+        // A page is the next 64 entries of a (request, query token)'s key
+        // list.  Four warps, one on each SM sub-partition, gather this CTA's
+        // chunks of the listed rows: warp gw takes rows 16 gw .. 16 gw + 15,
+        // eight lanes per row, one 16-byte cp.async per chunk and lane, into
+        // the page's stage in the 128-byte-swizzled layout the MMAs read.  A
+        // warp waits for its own copies, fences them for the tensor core,
+        // writes its 16 bits of the key mask and arrives on kv_full (four
+        // arrivals a page).  Padding, entries past the list and positions
+        // outside the cache read nothing (the row is zeros) and lose their
+        // bit.  A page's list entries are fetched two pages ahead.  The query
+        // pseudo-pages come by TMA, issued by warp 0 with the byte count; the
+        // other warps arrive on them plainly.  Every warp takes the stages in
+        // ring order, so each of its parity waits stays unambiguous, and
+        // holds no unsignalled page while it waits.  (More pages in flight
+        // per warp only lengthened each page's landing: random row reads
+        // saturate the memory system first.)
+        const int gw = warp - kGatherWarp0;
+        const uint64_t policy = policy_evict_first();
+        const int qrow0 = tile * kPairRows + static_cast<int>(rank) * kCtaRows;
+        const int uu = lane & 7, rq = lane >> 3;
+        const int n_ch = leader ? 5 : 4;
+        const int64_t tok_bytes = p.kv_token_bytes;
+        auto load_ix = [&](const Cursor& c) -> int {
+            const int t = c.blk * kPage + 16 * gw + (lane & 15);
+            return (c.valid && t < c.L) ? p.indices[static_cast<int64_t>(c.req) * p.topk + t] : -1;
+        };
+        auto acquire = [&](uint32_t n) -> bool {
+            return n < kStages ||
+                   warp_wait(&bars->kv_empty[n % kStages], ((n / kStages) + 1) & 1, wc);
+        };
+        Cursor ld = cursor_begin<true>(p, part);
+        Cursor pf = ld;
+        int ix_cur = load_ix(pf);
+        if (pf.valid) cursor_next<true>(p, part, pf);
+        int ix_next = load_ix(pf);
+        uint32_t n_issued = 0;
+        bool stop = false;
+        while (ld.valid && !stop) {
+            if (ld.blk == ld.b0) {
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t n = ld.ring() - 2 + e;
+                    const uint32_t st = n % kStages;
+                    if (!acquire(n)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        if (gw == 0) {
+                            uint8_t* dst = ring + st * kStageBytes;
+                            const int nl = e == 0 ? 5 : 4;
+                            mbar_arrive_expect_tx(&bars->kv_full[st], nl * kSlotBytes);
+                            for (int s = 0; s < nl; ++s)
+                                tma_load_3d(&q_map, &bars->kv_full[st], dst + s * kSlotBytes,
+                                            64 * (s == 4 ? kRopeChunk : rail_chunk(e, s)), qrow0,
+                                            ld.req, policy);
+                        } else {
+                            mbar_arrive(&bars->kv_full[st]);
+                        }
+                    }
+                    __syncwarp();
+                    n_issued = n + 1;
+                }
+                if (stop) break;
+            }
+            const uint32_t n = ld.ring();
+            const uint32_t st = n % kStages;
+            if (!acquire(n)) break;
+            uint8_t* stage = ring + st * kStageBytes;
+            if (!leader) {
+                // The peer's RoPE slot is zeros under a page (it held P or a
+                // query entry before).
+                uint4* z = reinterpret_cast<uint4*>(stage + 4 * kSlotBytes + 16 * gw * 128);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) z[lane + 32 * i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint32_t mask = 0;
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // row 4 j + rq of this warp's rows: the entry of lane 4 j + rq
+                const int ix = __shfl_sync(0xffffffffu, ix_cur, 4 * j + rq);
+                const bool v = ix >= 0 && static_cast<int64_t>(ix) < p.num_tokens;
+                bad |= static_cast<int64_t>(ix) >= p.num_tokens;
+                const uint8_t* src = p.kv_bytes + (v ? static_cast<int64_t>(ix) * tok_bytes : 0) + uu * 16;
+                const uint32_t dst = smem_u32(stage + sw128_offset(16 * gw + 4 * j + rq, uu));
+                const uint32_t nbytes = v ? 16u : 0u;
+                for (int s = 0; s < n_ch; ++s)
+                    cp_async_16(dst + s * kSlotBytes,
+                                src + 128 * (s == 4 ? kRopeChunk : rail_chunk(static_cast<int>(rank), s)),
+                                nbytes);
+                // rows 4 j .. 4 j + 3: the validity of lanes 0, 8, 16, 24
+                const uint32_t b = __ballot_sync(0xffffffffu, v);
+                mask |= ((b & 1u) | ((b >> 7) & 2u) | ((b >> 14) & 4u) | ((b >> 21) & 8u)) << (4 * j);
+            }
+            if (bad) atomicCAS(p.error_word, 0, MLA_ERR_BAD_INDEX);
+            n_issued = n + 1;
+            // The next page's entries are here; fetch the one after it.
+            ix_cur = ix_next;
+            if (pf.valid) cursor_next<true>(p, part, pf);
+            ix_next = load_ix(pf);
+            cursor_next<true>(p, part, ld);
+            cp_async_wait_all();
+            __syncwarp();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                key_mask16[4 * st + gw] = static_cast<uint16_t>(mask);
+                mbar_arrive(&bars->kv_full[st]);
+            }
+            __syncwarp();
+        }
+        // Drain: the query entries' copies have landed before warp 0 leaves.
+        if (gw == 0 && lane == 0)
+            for (uint32_t k = (n_issued >= kStages ? n_issued - kStages : 0); k < n_issued; ++k)
+                mbar_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, kDrainBudgetNs);
+        __syncwarp();
+    } else if (warp == kProducerWarp) {
+      if constexpr (!kSparse) {
         // ------------------------------------------------------ TMA producer
         // The whole warp walks the ring; lane 0 waits and issues the copies.
         // Block-table entries come through two 32-page windows in shared
@@ -341,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow0 = tile * kPairRows + static_cast<int>(rank) * kCtaRows;
         const int n_kv = leader ? 5 : 4;
         int32_t* bt_win = reinterpret_cast<int32_t*>(smem + kOffBt);
-        Cursor ld = cursor_begin(p, part), ahead = ld;
+        Cursor ld = cursor_begin<kSparse>(p, part), ahead = ld;
         auto fetch_window = [&](uint32_t slot) {
             int rq = -1, bk = 0;
             for (int i = 0; i < 32 && ahead.valid; ++i) {
@@ -349,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rq = ahead.req;
                     bk = ahead.blk;
                 }
-                cursor_next(p, part, ahead);
+                cursor_next<kSparse>(p, part, ahead);
             }
             if (rq >= 0)
                 cp_async_4(smem_u32(bt_win + 32 * slot + lane),
@@ -424,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fetch_window(1);
             else if ((ld.g & 31) == 31)
                 fetch_window((ld.g >> 5) & 1);
-            cursor_next(p, part, ld);
+            cursor_next<kSparse>(p, part, ld);
         }
         // Drain: no copy may still be landing when the CTA leaves.
         cp_async_wait_all();
@@ -432,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t k = (n_issued >= kStages ? n_issued - kStages : 0); k < n_issued; ++k)
                 mbar_drain(&bars->kv_full[k % kStages], (k / kStages) & 1, kDrainBudgetNs);
         __syncwarp();
+      }
     } else if (warp == kMmaWarp && !leader) {
         // ------------------------------------------- peer: landing forwarder
         // For every page the leader's MMAs will read, tell the leader that this
@@ -443,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // once the softmax warps copied them (q_copied, waited for before the
         // request's first page).  The next entry of a page's stage waits for
         // that page's PV, hence for this forwarding.
-        for (Cursor c = cursor_begin(p, part); c.valid; cursor_next(p, part, c)) {
+        for (Cursor c = cursor_begin<kSparse>(p, part); c.valid; cursor_next<kSparse>(p, part, c)) {
             const uint32_t n = c.ring();
             if (c.blk == c.b0 && !warp_wait(&bars->q_copied, c.item & 1, wc)) break;
             if (!warp_wait(&bars->kv_full[n % kStages], (n / kStages) & 1, wc)) break;
@@ -464,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQr = smem_desc(smem_u32(sQr), 16, 1024);
         const uint32_t tQ = tmem + kColQ, tS = tmem + kColS;
         uint32_t peer_par = 0;  // bit s: parity of the next kv_peer[s] phase
-        for (Cursor qk = cursor_begin(p, part); qk.valid; cursor_next(p, part, qk)) {
+        for (Cursor qk = cursor_begin<kSparse>(p, part); qk.valid; cursor_next<kSparse>(p, part, qk)) {
             const uint32_t n = qk.ring(), st = n % kStages;
             // (q_ready first: it also covers the landing of the request's
             // query entries, which share stages with its pages.)
@@ -504,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dV0 = smem_desc(smem_u32(ring), kSlotBytes, 1024);
         const uint64_t dP0 = smem_desc(smem_u32(ring + 4 * kSlotBytes), 16, 1024);
         const uint32_t tO = tmem + kColO;
-        for (Cursor pv = cursor_begin(p, part); pv.valid; cursor_next(p, part, pv)) {
+        for (Cursor pv = cursor_begin<kSparse>(p, part); pv.valid; cursor_next<kSparse>(p, part, pv)) {
             const bool first = pv.blk == pv.b0;
             if (!warp_poll(&bars->p_full[pv.g & 1], (pv.g >> 1) & 1, wc)) break;
             if (first && pv.item > 0 && !warp_poll(&bars->o_free, (pv.item - 1) & 1, wc)) break;
@@ -607,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int q_done = -1;
         for (int req = part.begin_req; req <= part.end_req; ++req) {
             int L, nb, b0, b1;
-            item_range(p, part, req, L, nb, b0, b1);
+            item_range<kSparse>(p, part, req, L, nb, b0, b1);
             int lim = L;
             if (p.causal) {
                 lim = L - p.s_q + s_idx + 1;
@@ -661,8 +792,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(pair_bar, 64);
                 const float4* xi = X + ((h * 2 + rho) * 4) * 64 + r;
                 float x[16];
-                const int t0 = blk * kPage + 32 * h + keep;
-                const int nvis = row_valid ? lim - t0 : 0;  // columns c < nvis are visible
+                // Column c (token 32 h + keep + c of the page) is visible when
+                // c < nvis (dense), or when bit c of keys, from the stage's
+                // key mask, is set (sparse; the page's kv_full phase completed
+                // before its S, so the wait only orders the mask read).
+                int nvis = 16;
+                uint32_t keys = 0xFFFFu;
+                if constexpr (kSparse) {
+                    wait(&bars->kv_full[st], ((gblk + 2 * item + 2) / kStages) & 1);
+                    keys = static_cast<uint32_t>(key_mask[st] >> (32 * h + keep)) & 0xFFFFu;
+                } else {
+                    const int t0 = blk * kPage + 32 * h + keep;
+                    nvis = row_valid ? lim - t0 : 0;
+                }
+                const bool whole = kSparse ? keys == 0xFFFFu : nvis >= 16;
                 const uint64_t sc2 = f32x2_splat(p.scale_log2);
                 float hmax = -INFINITY;
 #pragma unroll
@@ -676,13 +819,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Pages every valid row sees whole skip the masking (rows past
                 // the tile only feed their own, never written, output rows).
-                if (__all_sync(0xffffffffu, !row_valid || nvis >= 16)) {
+                if (__all_sync(0xffffffffu, !row_valid || whole)) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) hmax = fmaxf(hmax, x[c]);
                 } else {
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        x[c] = c < nvis ? x[c] : -INFINITY;
+                        x[c] = (kSparse ? ((keys >> c) & 1u) != 0 : c < nvis) ? x[c] : -INFINITY;
                         hmax = fmaxf(hmax, x[c]);
                     }
                 }
@@ -736,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Last page of the sequence: zero this CTA's V rows past its
                 // length (they may hold any bits, and 0 * NaN would poison PV).
-                if (blk == nb - 1 && (L & (kPage - 1)) != 0) {
+                if (!kSparse && blk == nb - 1 && (L & (kPage - 1)) != 0) {
                     const int tail0 = L & (kPage - 1);
                     const int per_slot = (kPage - tail0) * 8;  // 16-byte units
                     for (int i = stid; i < 4 * per_slot; i += kSoftmaxThreads) {
@@ -761,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this epilogue (this request's last QK^T is complete).
                 for (int nr = req + 1; nr <= part.end_req; ++nr) {
                     int L2, nb2, c0, c1;
-                    item_range(p, part, nr, L2, nb2, c0, c1);
+                    item_range<kSparse>(p, part, nr, L2, nb2, c0, c1);
                     if (c1 > c0) {
                         q_copy(gblk + 2 * (item + 1));
                         q_done = nr;
@@ -789,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = empty ? 0.f : 1.f / l_tot;
             const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
             const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
-            const OutMap om = out_map(req, row, p.h_q, p.s_q, 0, 1, p.h_q, p.out_sb, p.out_ss,
+            const OutMap om = out_map(req, row, p.h_q, p.s_q, kSparse ? p.fold : 0, 1, p.h_q, p.out_sb, p.out_ss,
                                       p.out_sh);
             const int dvb = 256 * h + 128 * rho;  // this thread's 128 output dims
             const bool write = row_valid && alive;
@@ -862,7 +1005,12 @@ cudaError_t duo_set_attributes() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(__atomic_load_n(&configured_mask, __ATOMIC_RELAXED) & (1 << dev))) {
-        e = cudaFuncSetAttribute(decode_duo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_duo_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(decode_duo_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
@@ -870,10 +1018,11 @@ cudaError_t duo_set_attributes() {
     return cudaSuccess;
 }
 
-void duo_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, cudaStream_t s) {
+void duo_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, int threads,
+                cudaStream_t s) {
     cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -895,10 +1044,10 @@ int duo_max_active_clusters() {
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    duo_config(cfg, attr, dim3(2, 1, 1), nullptr);
+    duo_config(cfg, attr, dim3(2, 1, 1), kThreads, nullptr);
     cfg.numAttrs = 1;  // the cluster shape only
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_duo_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_duo_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -911,8 +1060,11 @@ cudaError_t launch_decode_duo(const DecodeParams& p, const CUtensorMap& q_map,
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    duo_config(cfg, attr, dim3(2 * p.n_mtiles, p.num_parts, 1), stream);
-    return cudaLaunchKernelEx(&cfg, decode_duo_kernel, p, q_map, kv_map);
+    // (The sparse instantiation has four more warps; one CTA per SM either way.)
+    duo_config(cfg, attr, dim3(2 * p.n_mtiles, p.num_parts, 1),
+               p.sparse ? kThreadsSparse : kThreads, stream);
+    return p.sparse ? cudaLaunchKernelEx(&cfg, decode_duo_kernel<true>, p, q_map, kv_map)
+                    : cudaLaunchKernelEx(&cfg, decode_duo_kernel<false>, p, q_map, kv_map);
 }
 
 }  // namespace mla

@@ -1,6 +1,7 @@
 """Sparse decode ("[DeepSeek-3] FlashMLA", sec. 11: attention over per-query
 selected cache positions, index = page * 64 + offset) on the GPU against the
-fp64 sparse oracle, element by element.
+fp64 sparse oracle, element by element, on the automatic kernel choice (the
+CTA pair for lists of 128 or more query rows) and on the single-CTA kernel.
 Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3."""
 import numpy as np
 import pytest
@@ -28,13 +29,34 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
-def test_sparse_parity(case):
+@pytest.fixture
+def kernel_kind(request):
+    from decode_attention_paged_gb300 import api
+
+    default = api.get_decode_kernel()
+    api.set_decode_kernel(request.param)
+    yield request.param
+    api.set_decode_kernel(default)
+
+
+SPARSE_EXTRA = [
+    # lists of 128 and 256 rows on the CTA pair: ragged pages, heavy padding,
+    # splits over many parts, two tiles, several query tokens
+    (3, 2, 128, 700, 900, 0.3),
+    (2, 1, 256, 300, 400, 0.1),
+    (40, 1, 128, 1000, 1200, 0.0),
+]
+
+
+@pytest.mark.parametrize("kernel_kind", [3, 1], indirect=True, ids=["auto", "single"])
+@pytest.mark.parametrize("case", CASES + SPARSE_EXTRA,
+                         ids=[str(i) for i in range(len(CASES) + len(SPARSE_EXTRA))])
+def test_sparse_parity(kernel_kind, case):
     b, s_q, h_q, topk, ctx, pad = case
-    w = W.random_sparse_case(500 + CASES.index(case), b, s_q, h_q, topk, ctx, pad)
+    w = W.random_sparse_case(500 + (CASES + SPARSE_EXTRA).index(case), b, s_q, h_q, topk, ctx, pad)
     out, lse = run_gpu_sparse(w)
     ref_out, ref_lse = oracle.mla_sparse(sparse_problem(w), nthreads=NTHREADS)
-    assert_close(out, lse, ref_out, ref_lse, f"sparse {case}")
+    assert_close(out, lse, ref_out, ref_lse, f"sparse {case} kernel {kernel_kind}")
 
 
 def test_sparse_empty_lists():
