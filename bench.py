@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--kernel", choices=["auto", "single", "tq", "duo"], default="auto",
                     help="decode kernel: auto (default: tq for s_q*h_q <= 32, duo for >= 128, "
                          "else single), single CTA, Q in TMEM, or a CTA pair")
+    ap.add_argument("--sparse-only", action="store_true",
+                    help="time only the sparse-decode workload (steps/warmup as given) and "
+                         "print its line; for profiling")
     return ap.parse_args()
 
 
@@ -210,6 +213,30 @@ def kernel_of(kind, w):
         return kind
     R = w.s_q * w.h_q
     return "tq" if R <= 32 else ("duo" if R >= 128 else "single")
+
+
+def sparse_kernel_of(kind, h_q):
+    """Name of the decode kernel a sparse call with h_q query heads launches
+    (lists of h_q rows: the CTA pair where a dense call would take it, else
+    the single-CTA kernel)."""
+    return "duo" if (kind == "duo" or (kind == "auto" and h_q >= 128)) else "single"
+
+
+def sparse_line(w, r, kname, peaks, kx):
+    """Sparse-decode entry: step throughput, fractions of the peaks and the
+    DRAM traffic of the committed ncu summary when it matches the source."""
+    hbm_peak, bf16_peak = peaks[0], peaks[1]
+    t_s = r["ms_per_step"] * 1e-3
+    traffic = profile_traffic("sparse", kname)
+    return {
+        "workload": w.name, "kernel": KERNEL_SOURCES[kname][0] + " (row gather)",
+        "ms_per_step": r["ms_per_step"],
+        "step_tflops": r["flops"] / t_s / 1e12, "step_gbs": r["bytes"] / t_s / 1e9,
+        "frac_bf16_peak": r["flops"] / t_s / 1e12 / bf16_peak,
+        "frac_hbm_peak": r["bytes"] / t_s / 1e9 / hbm_peak,
+        "algorithmic_bytes": r["bytes"], "algorithmic_flops": r["flops"],
+        "traffic": traffic, "pieces": r["pieces"], "steps": kx,
+    }
 
 
 def roofline_of(res, workload, kname, peaks):
@@ -548,6 +575,16 @@ def main():
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "single": api.KERNEL_SINGLE,
                            "tq": api.KERNEL_TQ, "duo": api.KERNEL_DUO}[args.kernel])
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    if args.sparse_only:
+        if rank == 0:
+            ws = W_mod.sparse()
+            r = measure_sparse(ws, torch, api, W_mod, args.steps, args.warmup)
+            print(json.dumps({"sparse": sparse_line(ws, r, sparse_kernel_of(args.kernel, ws.h_q),
+                                                    (hbm_peak, bf16_peak), args.steps)}),
+                  flush=True)
+        if dist is not None:
+            dist.barrier()
+        return 0
     # weak scaling: every rank decodes its own batch of requests (replicas).
     w = replica_workload(W_mod, args.workload, rank)
     sampler = ClockSampler(list(range(world)) if world > 1 else [local]) if rank == 0 else None
@@ -648,14 +685,7 @@ def main():
         ws = W_mod.sparse()
         kx = max(50, min(args.steps, 1000))
         r = measure_sparse(ws, torch, api, W_mod, kx, 5)
-        t_s = r["ms_per_step"] * 1e-3
-        extra["sparse"] = {
-            "workload": ws.name, "ms_per_step": r["ms_per_step"],
-            "step_tflops": r["flops"] / t_s / 1e12, "step_gbs": r["bytes"] / t_s / 1e9,
-            "frac_bf16_peak": r["flops"] / t_s / 1e12 / bf16_peak,
-            "frac_hbm_peak": r["bytes"] / t_s / 1e9 / hbm_peak,
-            "pieces": r["pieces"], "steps": kx,
-        }
+        extra["sparse"] = sparse_line(ws, r, sparse_kernel_of(args.kernel, ws.h_q), peaks, kx)
         del ws
         torch.cuda.empty_cache()
 
