@@ -391,7 +391,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = nc * p.q_box_rows * 128;
         const bool sparse = p.sparse != 0;
+        // Dense: the part's first page's block-table entry is read at once,
+        // beside the first request's length, so page 0 waits for one load
+        // instead of the first window's walk and its copy.  Used when the
+        // cursor does start there (a part may begin on a request with no
+        // blocks).
+        const bool bt0_ok = !p.sparse && part.begin_req <= part.end_req &&
+                            part.begin_block >= 0 && part.begin_block < p.max_blocks;
+        const int bt0 = bt0_ok ? p.block_table[static_cast<int64_t>(part.begin_req / kvh) * p.bt_stride +
+                                               part.begin_block]
+                               : 0;
         Cursor ld = cursor_begin<kHeads>(p, part), ahead = ld;
+        const bool direct0 = bt0_ok && ld.valid && ld.req == part.begin_req && ld.blk == part.begin_block;
         auto fetch_window = [&](uint32_t slot) {
             int rq = -1, bk = 0;
             for (int i = 0; i < 32 && ahead.valid; ++i) {
@@ -431,17 +442,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++n_q;
         };
         if (ld.valid) issue_q(ld.req);
-        if (!sparse) fetch_window(0);
+        if (!sparse && !direct0) fetch_window(0);
         while (ld.valid) {
             if (!sparse) {
                 // Window (g / 32) has landed: the first waits for its only
-                // group, later ones leave the next window's group pending.
-                if (ld.g == 0)
-                    cp_async_wait_group<0>();
-                else if ((ld.g & 31) == 0)
-                    cp_async_wait_group<1>();
-                __syncwarp();
-                const int page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
+                // group (for both windows' groups, minus the second, when page
+                // 0 came direct), later ones leave the next window's group
+                // pending.
+                int page = bt0;
+                if (!(direct0 && ld.g == 0)) {
+                    if (ld.g == 0)
+                        cp_async_wait_group<0>();
+                    else if ((ld.g & 31) == 0 || (direct0 && ld.g == 1))
+                        cp_async_wait_group<1>();
+                    __syncwarp();
+                    page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
+                }
                 const int st = ld.g & 1;
                 if (ld.g >= 2 && !warp_wait(&bars->kv_empty[st], ((ld.g >> 1) + 1) & 1, wc)) break;
                 if (lane == 0) {
@@ -483,11 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(&bars->q_empty, (ld.item - 1) & 1, wc)) break;
                 issue_q(ld.req);
             }
-            // After page 0: the second window; after the last page of window
-            // w: window w + 2 into w's slot (every lane has read its entry).
+            // After page 0: the first window (when page 0 came direct) and the
+            // second; after the last page of window w: window w + 2 into w's
+            // slot (every lane has read its entry).
             if (!sparse) {
-                if (ld.g == 0)
+                if (ld.g == 0) {
+                    if (direct0) fetch_window(0);
                     fetch_window(1);
+                }
                 else if ((ld.g & 31) == 31)
                     fetch_window((ld.g >> 5) & 1);
             }

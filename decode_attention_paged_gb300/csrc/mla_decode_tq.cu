@@ -310,7 +310,18 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = kChunks * p.q_box_rows * 128;
         int32_t* bt_win = reinterpret_cast<int32_t*>(smem + lay.off_bt);
+        // The part's first page: its block-table entry is read at once, beside
+        // the first request's length, so page 0 waits for one load instead of
+        // the first window's walk (which reads the lengths of the requests it
+        // crosses) and its copy.  Used when the cursor does start there (a
+        // part may begin on a request with no blocks, which it skips).
+        const bool bt0_ok = part.begin_req <= part.end_req && part.begin_block >= 0 &&
+                            part.begin_block < p.max_blocks;
+        const int bt0 = bt0_ok ? p.block_table[static_cast<int64_t>(part.begin_req) * p.bt_stride +
+                                               part.begin_block]
+                               : 0;
         Cursor ld = cursor_begin(p, part), ahead = ld;
+        const bool direct0 = bt0_ok && ld.valid && ld.req == part.begin_req && ld.blk == part.begin_block;
         auto fetch_window = [&](uint32_t slot) {
             int rq = -1, bk = 0;
             for (int i = 0; i < 32 && ahead.valid; ++i) {
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             issue_q(0, ld.req);
             n_issued = 1;
         }
-        fetch_window(0);
+        if (!direct0) fetch_window(0);
         bool stop = false;
         while (ld.valid && !stop) {
             // First block of a request: its Q tile goes into the ring first
@@ -364,14 +375,20 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                 }
                 int page = 0;
                 if (entry == 1) {
-                    // Window (g / 32) has landed: the first waits for its only
-                    // group, later ones leave the next window's group pending.
-                    if (ld.g == 0)
-                        cp_async_wait_group<0>();
-                    else if ((ld.g & 31) == 0)
-                        cp_async_wait_group<1>();
-                    __syncwarp();
-                    page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
+                    if (direct0 && ld.g == 0) {
+                        page = bt0;
+                    } else {
+                        // Window (g / 32) has landed: the first waits for its
+                        // only group (for both windows' groups, minus the
+                        // second, when page 0 came direct); later ones leave
+                        // the next window's group pending.
+                        if (ld.g == 0)
+                            cp_async_wait_group<0>();
+                        else if ((ld.g & 31) == 0 || (direct0 && ld.g == 1))
+                            cp_async_wait_group<1>();
+                        __syncwarp();
+                        page = bt_win[32 * ((ld.g >> 5) & 1) + (ld.g & 31)];
+                    }
                 }
                 if (entry == 0) {
                     issue_q(st, ld.req);
@@ -406,10 +423,13 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                 n_issued = n + 1;
             }
             if (stop) break;
-            // After page 0: the second window; after the last page of window
-            // w: window w + 2 into w's slot (every lane has read its entry).
-            if (ld.g == 0)
+            // After page 0: the first window (when page 0 came direct) and the
+            // second; after the last page of window w: window w + 2 into w's
+            // slot (every lane has read its entry).
+            if (ld.g == 0) {
+                if (direct0) fetch_window(0);
                 fetch_window(1);
+            }
             else if ((ld.g & 31) == 31)
                 fetch_window((ld.g >> 5) & 1);
             cursor_next(p, part, ld);
