@@ -507,15 +507,15 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             tc_fence_after();
             const uint64_t bV = dV0 + st * kStageUnits;
             const uint64_t dP = dP0 + st * kStageUnits;
+            // One elected thread issues the whole burst and commits it.
+            if (elect_one()) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    if (elect_one())
+                    for (int kk = 0; kk < 4; ++kk)
                         mma_ws_ss(tmem + kColO + 128 * h, dP + 2 * kk,
                                   bV + h * kHalfUnits + 128 * kk, idesc_pv,
                                   (first && kk == 0) ? 0u : 1u);
-            if (elect_one()) {
                 mma_commit(&bars->pv_done[pv.g & 1]);
                 mma_commit(&bars->kv_empty[st]);
             }
