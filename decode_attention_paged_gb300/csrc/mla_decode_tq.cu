@@ -419,6 +419,12 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                     }
                     __syncwarp();
                     page_bits |= 1u << st;
+                    // First page of a request: ask L2 for the next request's
+                    // Q tile, which its ring entry will load after this
+                    // request's last page.
+                    if (ld.blk == ld.b0 && ld.req < part.end_req && lane == 0)
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_prefetch_l2_3d(&q_map, 64 * c, mtile * kTileM, ld.req + 1);
                 }
                 n_issued = n + 1;
             }
@@ -776,13 +782,11 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             const float lse2 = empty ? -INFINITY : m_used + fast_log2(l_tot);
             const int64_t acc_row = static_cast<int64_t>(slot) * p.R + row;
             if (has_blocks) {
-#pragma unroll 1
-                for (int cg = 0; cg < 8; ++cg) {
-                    uint32_t o[32];
-                    tmem_ld32(tl + kColO + 32 * cg, o);
-                    tmem_ld_wait();
+                // Column groups per TMEM wait: two with the FP8 cache (measured
+                // faster there), one for bf16 (two slowed it).
+                constexpr int kGroups = kFp8 ? 2 : 1;
+                auto store_cg = [&](int cg, const uint32_t (&o)[32]) {
                     const int dv0 = 256 * (cg >> 2) + 128 * half + 32 * (cg & 3);
-                    if (!row_valid) continue;
                     if (split) {
                         float4* dst = reinterpret_cast<float4*>(p.oaccum + acc_row * kDv + dv0);
 #pragma unroll
@@ -804,6 +808,16 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
+                };
+#pragma unroll 1
+                for (int cg = 0; cg < 8; cg += kGroups) {
+                    uint32_t o[kGroups][32];
+#pragma unroll
+                    for (int k = 0; k < kGroups; ++k) tmem_ld32(tl + kColO + 32 * (cg + k), o[k]);
+                    tmem_ld_wait();
+                    if (!row_valid) continue;
+#pragma unroll
+                    for (int k = 0; k < kGroups; ++k) store_cg(cg + k, o[k]);
                 }
                 tc_fence_before();
                 warp_arrive(&bars->o_free);
