@@ -12,12 +12,13 @@ the benchmark's definition (TFLOP/s and HBM GB/s of algorithmic work, as a
 fraction of the measured BF16 / HBM peaks).
 
 Timing (rank-local, then max over ranks):
-  * timed region (`value`): K back-to-back replays of a CUDA graph holding one
-    step exactly as a user calls it (programmatic launch between the kernels
-    intact), bracketed by a barrier and a device synchronisation; CUDA events
-    on the replay stream.  No L2 flush between replays: the inputs (~300 MB of
-    KV pages) exceed the 129 MB L2;
-  * flushed step: up to 2000 replays of the same graph, each preceded by a
+  * timed region (`value`): K back-to-back steps, each exactly the call a
+    user makes, launched as CUDA graphs of 8 consecutive calls (as a model's
+    layers issue them; programmatic launch overlaps each call with the one
+    before, inside a graph), bracketed by a barrier and a device
+    synchronisation; CUDA events on the replay stream.  No L2 flush between
+    steps: the inputs (~300 MB of KV pages) exceed the 129 MB L2;
+  * flushed step: up to 2000 replays of a graph of one step, each preceded by a
     write of twice the L2 size outside the events, so that every step starts
     with a cold L2 (`step_l2_flushed`);
   * kernel region: K steps (at most 2000) with the three kernels launched as
@@ -288,9 +289,28 @@ def capture(torch, fn):
     return gr
 
 
-def time_steps(torch, graph, K, W, dist=None):
-    for _ in range(W):
-        graph.replay()
+CALLS_PER_GRAPH = 8
+
+
+def time_calls(torch, fn, K, W, dist=None):
+    """Time exactly K calls of fn (one step each), launched as CUDA graphs of
+    CALLS_PER_GRAPH consecutive calls -- the way a model's layers issue them
+    back to back, so that programmatic launch overlaps each call with the
+    previous one -- plus one graph of the remainder.  At least W calls of
+    warm-up.  Returns (ms for the K calls, wall-clock window)."""
+    G = max(1, min(CALLS_PER_GRAPH, K))
+
+    def calls(n):
+        def run():
+            for _ in range(n):
+                fn()
+        return run
+
+    gr = capture(torch, calls(G))
+    rem = K - (K // G) * G
+    gr_rem = capture(torch, calls(rem)) if rem else None
+    for _ in range((W + G - 1) // G):
+        gr.replay()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -299,13 +319,16 @@ def time_steps(torch, graph, K, W, dist=None):
     e1 = torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     e0.record()
-    for _ in range(K):
-        graph.replay()
+    for _ in range(K // G):
+        gr.replay()
+    if gr_rem is not None:
+        gr_rem.replay()
     e1.record()
     torch.cuda.synchronize()
     t1 = time.time()
     if dist is not None:
         dist.barrier()
+    del gr, gr_rem
     return e0.elapsed_time(e1), (t0, t1)
 
 
@@ -361,7 +384,7 @@ def measure_workload(w, torch, api, W_mod, K, Wup, dist=None):
     gr_split = capture(torch, call.splitkv)
     gr_comb = capture(torch, call.combine)
     assert api.mla_last_device_error() == 0
-    ms_total, win1 = time_steps(torch, gr_full, K, Wup, dist)
+    ms_total, win1 = time_calls(torch, full_step, K, Wup, dist)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     flush.zero_()
     kt, k_used, win2 = time_kernels(torch, gr_sched, gr_split, gr_comb, K, flush)
@@ -386,14 +409,12 @@ def measure_sparse(w, torch, api, W_mod, K, Wup):
     g = w.to("cuda")
     meta, ns = api.mla_get_metadata_sparse(w.topk, w.b, w.h_q, w.s_q)
     call = api.SparseDecodeCall(g.q, g.k_cache, g.indices, w.softmax_scale, meta, ns)
-    gr = capture(torch, call.fwd)
-    assert api.mla_last_device_error() == 0
-    ms_total, _ = time_steps(torch, gr, K, Wup)
+    ms_total, _ = time_calls(torch, call.fwd, K, Wup)
     code = api.mla_last_device_error()
     assert code == 0, f"device error {code}"
     res = {"ms_per_step": ms_total / K, "flops": W_mod.sparse_flops(w.indices, w.h_q),
            "bytes": W_mod.sparse_hbm_bytes(w.indices, w.h_q), "pieces": int(ns[-1].item())}
-    del gr, call, g
+    del call, g
     return res
 
 
@@ -404,15 +425,13 @@ def measure_fp8(w, torch, api, W_mod, K, Wup):
     meta, ns = api.mla_get_metadata(g.cache_seqlens, w.h_q, w.s_q)
     call = api.Fp8DecodeCall(g.q, g.k_cache, g.block_table, g.cache_seqlens, w.softmax_scale,
                              w.causal, meta, ns)
-    gr = capture(torch, call.fwd)
-    assert api.mla_last_device_error() == 0
-    ms_total, _ = time_steps(torch, gr, K, Wup)
+    ms_total, _ = time_calls(torch, call.fwd, K, Wup)
     code = api.mla_last_device_error()
     assert code == 0, f"device error {code}"
     sl = w.cache_seqlens.tolist()
     res = {"ms_per_step": ms_total / K, "flops": W_mod.flops(sl, w.s_q, w.h_q, w.causal),
            "bytes": W_mod.fp8_hbm_bytes(sl, w.s_q, w.h_q), "tokens": sum(sl)}
-    del gr, call, g
+    del call, g
     return res
 
 
@@ -668,8 +687,7 @@ def main():
         meta_h, ns_h = api.mla_get_metadata(gh.cache_seqlens, wh.h_q, wh.s_q, wh.h_kv)
         call_h = api.DecodeCall(gh.q, gh.k_cache, gh.block_table, gh.cache_seqlens,
                                 wh.softmax_scale, wh.causal, meta_h, ns_h)
-        gr_h = capture(torch, call_h.fwd)
-        ms_h, _ = time_steps(torch, gr_h, kx, 5)
+        ms_h, _ = time_calls(torch, call_h.fwd, kx, 5)
         assert api.mla_last_device_error() == 0
         t_s = ms_h / kx * 1e-3
         sl = wh.cache_seqlens.tolist()
@@ -680,7 +698,7 @@ def main():
             "step_gbs": bytes_h / t_s / 1e9, "step_tflops": flops_h / t_s / 1e12,
             "frac_hbm_peak": bytes_h / t_s / 1e9 / hbm_peak, "steps": kx,
         }
-        del gr_h, call_h, gh, wh
+        del call_h, gh, wh
         torch.cuda.empty_cache()
         ws = W_mod.sparse()
         kx = max(50, min(args.steps, 1000))
@@ -696,9 +714,10 @@ def main():
         "config": {"workload": w.name, "batch": w.b, "s_q": w.s_q, "h_q": w.h_q,
                    "seqlen": int(w.cache_seqlens.max()), "page": 64, "d_qk": 576, "d_v": 512,
                    "causal": w.causal, "parallelism": f"replicas x{world}",
-                   "l2": "value: back-to-back step replays, inputs larger than L2 (KV 302 MB "
+                   "l2": "value: back-to-back steps, inputs larger than L2 (KV 302 MB "
                          "vs 129 MB); step_l2_flushed and roofline: L2 flushed before each "
-                         "step / launch"},
+                         "step / launch",
+                   "launch": f"steps as CUDA graphs of {CALLS_PER_GRAPH} consecutive calls"},
         "tflops": tflops, "frac_hbm_peak_step": gbs / world / hbm_peak,
         "step_l2_flushed": flushed,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

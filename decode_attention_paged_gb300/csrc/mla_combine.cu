@@ -58,18 +58,43 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineParams p) {
     // The next decode grid may launch now: it waits for this grid's completion
     // before it reads its plan or writes anything.
     pdl_launch_dependents();
-    pdl_wait_primary();
-    // Metadata built for another shape: the decode kernel has already recorded
+    // The plan is read before the wait: the decode grid lets this grid launch
+    // only after its own wait, when the plan was already complete.  Metadata
+    // built for another shape: the decode kernel has already recorded
     // MLA_ERR_METADATA_MISMATCH; num_splits may be too short to index.  (Every
     // condition below is the same for all warps of a CTA, or for all warps of
     // a row: no warp leaves while its row's partners still need the barrier.)
-    if (ld_i(p.meta + kHMagic) != kMetaMagic || ld_i(p.meta + kHBatch) != p.batch ||
-        ld_i(p.meta + kHRows) != p.R)
-        return;
-    const int first = ld_i(p.num_splits + req);
-    const int n = ld_i(p.num_splits + req + 1) - first;
-    if (n <= 1) return;  // the decode kernel wrote this request directly
+    const bool plan_ok = ld_i(p.meta + kHMagic) == kMetaMagic &&
+                         ld_i(p.meta + kHBatch) == p.batch && ld_i(p.meta + kHRows) == p.R;
+    int first = 0, n = 0;
+    if (plan_ok) {
+        first = ld_i(p.num_splits + req);
+        n = ld_i(p.num_splits + req + 1) - first;
+    }
+    pdl_wait_primary();
+    // A request cut into one piece was written by the decode kernel directly.
+    if (n <= 1) return;
     const bool row_ok = row < p.R;
+    const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
+    const int64_t piece_stride = static_cast<int64_t>(p.R) * kDv;
+    const int mine = n > j ? (n - j + kW - 1) / kW : 0;  // pieces of this warp
+    // Partial rows of this warp's pieces base + u (u < 4), 16 floats per lane.
+    float4 x[4][4];
+    auto load_group = [&](int base) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (base + u < mine) {
+                const float* src = o_base + static_cast<int64_t>(j + kW * (base + u)) * piece_stride;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) x[u][v] = ld_f4(src + 4 * v);
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+    // The first group's loads go out with the lse loads below.
+    if (row_ok) load_group(0);
 
     // The largest piece lse of the row (every warp of the row computes it).
     const float* lse_base = p.lseaccum + static_cast<int64_t>(first) * p.R + row;
@@ -84,13 +109,10 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineParams p) {
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (row_ok && mx != -INFINITY) {
-        const float* o_base = p.oaccum + (static_cast<int64_t>(first) * p.R + row) * kDv + lane * 16;
-        const int64_t piece_stride = static_cast<int64_t>(p.R) * kDv;
         // Pieces j, j + kW, ...: lane t of each group of 32 holds piece
         // j + kW (base + t)'s weight; the partial rows are streamed with four
         // pieces' loads in flight.  An empty piece (lse = -inf) has weight 0
         // and an all-zero partial row.
-        const int mine = n > j ? (n - j + kW - 1) / kW : 0;  // pieces of this warp
         for (int base = 0; base < mine; base += 32) {
             const int t = base + lane;
             const float lk = t < mine ? ld_f(lse_base + static_cast<int64_t>(j + kW * t) * p.R) : -INFINITY;
@@ -101,22 +123,13 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineParams p) {
             wsum += ws;
             const int m = min(32, mine - base);
             for (int j0 = 0; j0 < m; j0 += 4) {
-                float4 x[4][4];
                 float w[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     w[u] = __shfl_sync(0xffffffffu, wl, (j0 + u) & 31);
-                    if (j0 + u < m) {
-                        const float* src =
-                            o_base + static_cast<int64_t>(j + kW * (base + j0 + u)) * piece_stride;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) x[u][v] = ld_f4(src + 4 * v);
-                    } else {
-                        w[u] = 0.f;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+                    if (j0 + u >= m) w[u] = 0.f;
                 }
+                if (base + j0 > 0) load_group(base + j0);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -178,13 +191,16 @@ __global__ void __launch_bounds__(128) combine_dims_kernel(CombineParams p) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int req = blockIdx.y, row = blockIdx.x * 4 + warp;
     pdl_launch_dependents();
+    // The plan is read before the wait (see combine_kernel).
+    const bool plan_ok = ld_i(p.meta + kHMagic) == kMetaMagic &&
+                         ld_i(p.meta + kHBatch) == p.batch && ld_i(p.meta + kHRows) == p.R;
+    int first = 0, n = 0;
+    if (plan_ok) {
+        first = ld_i(p.num_splits + req);
+        n = ld_i(p.num_splits + req + 1) - first;
+    }
     pdl_wait_primary();
-    if (ld_i(p.meta + kHMagic) != kMetaMagic || ld_i(p.meta + kHBatch) != p.batch ||
-        ld_i(p.meta + kHRows) != p.R || row >= p.R)
-        return;
-    const int first = ld_i(p.num_splits + req);
-    const int n = ld_i(p.num_splits + req + 1) - first;
-    if (n <= 1) return;
+    if (row >= p.R || n <= 1) return;
     const int dv = p.dv, nd = dv / 32;
     const float* lse_base = p.lseaccum + static_cast<int64_t>(first) * p.R + row;
     float mx = -INFINITY;

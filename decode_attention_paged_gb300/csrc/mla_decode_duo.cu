@@ -305,10 +305,11 @@ __global__ void __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // The dependent (combine) grid may launch now: it waits for this grid's
-    // completion before it reads anything (griddepcontrol.wait).
-    pdl_launch_dependents();
     pdl_wait_primary();
+    // The dependent (combine) grid may launch now.  It waits for this grid's
+    // completion before it reads the partials; the plan, final once the wait
+    // above returned, it may read at once.
+    pdl_launch_dependents();
 
     bool ok = (smem_u32(smem) & 1023u) == 0;
     const int32_t* hdr = p.meta;
