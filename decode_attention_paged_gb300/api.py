@@ -17,6 +17,17 @@ from . import _lib
 
 D_QK = 576
 D_V = 512
+# Smallest metadata buffer a decode call accepts: the header and room for 256
+# part records (mla_metadata_size never returns less).
+META_MIN_INTS = 8 + 8 * 256
+
+
+def _check_plan(meta: torch.Tensor, num_splits: torch.Tensor) -> None:
+    assert meta.dtype == torch.int32 and num_splits.dtype == torch.int32
+    assert meta.is_contiguous() and meta.numel() >= META_MIN_INTS, \
+        "meta must be a buffer of mla_metadata_size() bytes"
+
+
 PAGE = 64
 
 
@@ -75,6 +86,7 @@ class DecodeCall:
                  num_splits, workspace=None, out=None, lse=None, stream=None):
         assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
         assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+        _check_plan(meta, num_splits)
         b, s_q, h_q, d = q.shape
         assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
             q.stride(1) == h_q * D_QK, \
@@ -150,7 +162,7 @@ def mla_decode_fwd_dims(q: torch.Tensor, k_cache: torch.Tensor, block_table: tor
     of 64, head_dim_v <= min(d, 512), d <= 576)."""
     assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
     assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
-    assert meta.dtype == torch.int32 and num_splits.dtype == torch.int32
+    _check_plan(meta, num_splits)
     b, s_q, h_q, d = q.shape
     assert q.stride(3) == 1 and q.stride(2) == d and q.stride(1) == h_q * d, \
         "q rows must be packed: [b][s_q][h_q][d] with the (s_q, h_q) rows contiguous"
@@ -188,7 +200,7 @@ def mla_decode_fwd_noalloc(q: torch.Tensor, k_cache: torch.Tensor, block_table: 
     allocates."""
     assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
     assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
-    assert meta.dtype == torch.int32 and num_splits.dtype == torch.int32
+    _check_plan(meta, num_splits)
     b, s_q, h_q, d = q.shape
     assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and q.stride(1) == h_q * D_QK
     num_pages, page, h_kv, dk = k_cache.shape
@@ -221,6 +233,7 @@ class Fp8DecodeCall:
                  num_splits, workspace=None, out=None, lse=None, stream=None):
         assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.uint8
         assert block_table.dtype == torch.int32 and cache_seqlens.dtype == torch.int32
+        _check_plan(meta, num_splits)
         b, s_q, h_q, d = q.shape
         assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
             q.stride(1) == h_q * D_QK
@@ -312,6 +325,7 @@ class SparseDecodeCall:
                  out=None, lse=None, stream=None):
         assert q.dtype == torch.bfloat16 and k_cache.dtype == torch.bfloat16
         assert indices.dtype == torch.int32 and indices.is_contiguous()
+        _check_plan(meta, num_splits)
         b, s_q, h_q, d = q.shape
         assert d == D_QK and q.stride(3) == 1 and q.stride(2) == D_QK and \
             q.stride(1) == h_q * D_QK

@@ -274,7 +274,7 @@ int mla_metadata_size(int batch, int h_q, int s_q, int h_kv, size_t* meta_bytes,
     if ((st = device_info(&d))) return st;
     const Geo g = geo_of(batch, h_q, s_q, h_kv);
     const int parts = num_parts_of(g.R, h_kv, d);
-    if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
+    if (meta_bytes) *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts > kMetaMinParts ? parts : kMetaMinParts) * kMetaFields);
     if (num_splits_bytes) *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(g.nreq) + 1);
     return MLA_OK;
 }
@@ -579,7 +579,7 @@ int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t* meta
     if ((st = device_info(&d))) return st;
     const int parts = num_parts_sparse(h_q, d);
     if (meta_bytes)
-        *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts) * kMetaFields);
+        *meta_bytes = sizeof(int32_t) * (kMetaHeader + static_cast<size_t>(parts > kMetaMinParts ? parts : kMetaMinParts) * kMetaFields);
     if (num_splits_bytes)
         *num_splits_bytes = sizeof(int32_t) * (static_cast<size_t>(batch) * s_q + 1);
     return MLA_OK;

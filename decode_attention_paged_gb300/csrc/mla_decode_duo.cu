@@ -313,17 +313,32 @@ __global__ void __launch_bounds__(kSparse ? kThreadsSparse : kThreads, 1)
 
     bool ok = (smem_u32(smem) & 1023u) == 0;
     const int32_t* hdr = p.meta;
+    // The part record is read beside the header: every metadata buffer has
+    // room for kMetaMinParts records, and the record is used only once the
+    // header matches this call.
+    static_assert(kBeginReq == 0 && kEndReq == 1 && kBeginBlock == 2 && kEndBlock == 3 &&
+                      kBeginSplit == 4,
+                  "record fields 0..4");
+    const int32_t* rec = hdr + kMetaHeader + part_idx * kMetaFields;
+    int32_t rv[5] = {0, 0, 0, 0, 0};
+    if (part_idx < kMetaMinParts) {
+#pragma unroll
+        for (int f = 0; f < 5; ++f) rv[f] = rec[f];
+    }
     if (ok && (hdr[kHMagic] != kMetaMagic || hdr[kHBatch] != p.batch || hdr[kHRows] != p.R ||
                hdr[kHParts] != p.num_parts || hdr[kHPage] != kPage))
         ok = false;
     Part part{};
     if (ok) {
-        const int32_t* rec = hdr + kMetaHeader + part_idx * kMetaFields;
-        part.begin_req = rec[kBeginReq];
-        part.end_req = rec[kEndReq];
-        part.begin_block = rec[kBeginBlock];
-        part.end_block = rec[kEndBlock];
-        part.begin_split = rec[kBeginSplit];
+        if (part_idx >= kMetaMinParts) {
+#pragma unroll
+            for (int f = 0; f < 5; ++f) rv[f] = rec[f];
+        }
+        part.begin_req = rv[kBeginReq];
+        part.end_req = rv[kEndReq];
+        part.begin_block = rv[kBeginBlock];
+        part.end_block = rv[kEndBlock];
+        part.begin_split = rv[kBeginSplit];
         if (part.begin_req < p.batch &&
             (part.begin_req < 0 || part.end_req >= p.batch || part.end_req < part.begin_req))
             ok = false;

@@ -19,6 +19,10 @@ constexpr int kChunks = kDqk / 64;  // 64-dim chunks of one row: 9
 constexpr int kChunkBytes = 64 * 128;  // one [64 rows][64 dims] bf16 chunk, 128B-swizzled
 constexpr int kMetaHeader = 8;   // int32 header words before the part records
 constexpr int kMetaFields = 8;   // int32 words per part record
+// Every metadata buffer has room for at least this many part records, so a
+// decode CTA with a smaller part index may read its record beside the header
+// (and use it only once the header matches).
+constexpr int kMetaMinParts = 256;
 constexpr int kMetaMagic = 0x4D4C4131;  // "MLA1"
 
 // Part record fields (the DecodingSchedMeta of the Tile Scheduler section).

@@ -94,8 +94,10 @@ MLA_API int mla_version(void);
  * mla_metadata_size -- bytes of the two metadata buffers for a problem shape.
  * Source: "FlashMLA 新内核深度解析", section "Tile Scheduler" (DecodingSchedMeta
  * per SM part, num_splits per request).
- *   meta_bytes: int32 header[8] + num_sm_parts records of 8 int32 each, where
- *     num_sm_parts = max(1, SMs / ceil(s_q*h_q / h_kv / 64)) on the current device;
+ *   meta_bytes: int32 header[8] + max(num_sm_parts, 256) records of 8 int32
+ *     each, where num_sm_parts = max(1, SMs / ceil(s_q*h_q / h_kv / 64)) on the
+ *     current device (records past num_sm_parts are not written; the room lets
+ *     a decode CTA read its record before it has checked the header);
  *   num_splits_bytes: int32[batch + 1].
  * With h_kv > 1 the plan's requests are the (request, cache head) pairs:
  * num_splits is int32[batch * h_kv + 1] and a tile has s_q*h_q/h_kv rows.

@@ -20,7 +20,8 @@ def device_plan(seqlens, h_q, s_q):
     meta, ns = api.mla_get_metadata(sl, h_q, s_q)
     torch.cuda.synchronize()
     meta = meta.cpu().numpy()
-    return meta[:HEADER], meta[HEADER:].reshape(-1, 8), ns.cpu().numpy()
+    num_parts = int(meta[3])  # the buffer has room for more records than the plan writes
+    return meta[:HEADER], meta[HEADER:HEADER + 8 * num_parts].reshape(-1, 8), ns.cpu().numpy()
 
 
 CASES = [

@@ -142,7 +142,7 @@ def _noalloc_args(**override):
         block_table=torch.zeros(b, 2, dtype=torch.int32),
         cache_seqlens=torch.full((b,), 64, dtype=torch.int32),
         softmax_scale=576 ** -0.5, causal=False,
-        meta=torch.zeros(8 + 8 * 152, dtype=torch.int32),
+        meta=torch.zeros(8 + 8 * 256, dtype=torch.int32),
         num_splits=torch.zeros(b + 1, dtype=torch.int32),
         out=torch.zeros(b, s_q, h_q, 512, dtype=torch.bfloat16),
         lse=torch.zeros(b, h_q, s_q, dtype=torch.float32))
