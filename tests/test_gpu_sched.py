@@ -112,3 +112,15 @@ def test_default_overhead_follows_the_kernel():
     # one 128-row tile: the CTA-pair kernel (two 64-row tiles if its clusters
     # cannot be resident and the single-CTA kernel runs instead)
     assert int(hdr[5]) == (5 if int(hdr[4]) == 1 else 2)
+
+
+def test_metadata_has_room_for_256_records():
+    """Decode CTAs read their part record beside the header: every metadata
+    buffer the library sizes holds the header and at least 256 records."""
+    from decode_attention_paged_gb300 import api
+
+    for shape in ((1, 16, 1, 1), (64, 128, 1, 1), (32, 64, 1, 4), (128, 128, 2, 1)):
+        mb, _ = api.metadata_size(*shape)
+        assert mb >= 4 * (8 + 8 * 256)
+        mbs, _ = api.metadata_size_sparse(shape[0], shape[1], shape[2])
+        assert mbs >= 4 * (8 + 8 * 256)

@@ -173,3 +173,29 @@ def test_noalloc_wrapper_rejects_wrong_dtypes_and_shapes(bad):
         a[key] = torch.zeros(2, 1, 16, dtype=torch.float32)
     with pytest.raises(AssertionError):
         api.mla_decode_fwd_noalloc(**a)
+
+
+def test_decode_wrappers_refuse_metadata_below_the_floor():
+    """A decode CTA may read its part record before it has checked the plan
+    header, which is in bounds because every metadata buffer holds room for
+    256 records.  The Python wrappers refuse a smaller buffer before any
+    device call."""
+    import torch
+
+    from decode_attention_paged_gb300 import api
+
+    small = torch.zeros(8 + 8 * 152, dtype=torch.int32)
+    a = _noalloc_args(meta=small)
+    with pytest.raises(AssertionError):
+        api.mla_decode_fwd_noalloc(**a)
+    with pytest.raises(AssertionError):
+        api.DecodeCall(a["q"], a["k_cache"], a["block_table"], a["cache_seqlens"],
+                       a["softmax_scale"], False, small, a["num_splits"])
+    with pytest.raises(AssertionError):
+        api.mla_decode_fwd_dims(a["q"], a["k_cache"], a["block_table"], a["cache_seqlens"],
+                                a["softmax_scale"], False, small, a["num_splits"], 512)
+    idx = torch.zeros(2, 1, 64, dtype=torch.int32)
+    with pytest.raises(AssertionError):
+        api.SparseDecodeCall(a["q"], a["k_cache"], idx, a["softmax_scale"], small,
+                             a["num_splits"])
+    assert api.META_MIN_INTS == 8 + 8 * 256
