@@ -355,7 +355,10 @@ MLA_API int mla_decode_fp8_fwd(const void *q_dev, int64_t q_batch_stride, const 
  *   out_dev, lse_dev as mla_decode_fwd.
  * Constraints: batch * s_q <= 16384, 0 <= topk <= 2^24, h_kv = 1.
  * Enqueues the decode kernel and the combine kernel on `stream`;
- * graph-capturable.
+ * graph-capturable.  The decode kernel is the CTA pair when the dense
+ * choice for a tile of h_q rows is the pair (by default h_q >= 128; see
+ * mla_set_decode_kernel), else the single-CTA kernel (the TQ kernel does no
+ * row gather); mla_get_metadata_sparse plans for the same kernel.
  */
 MLA_API int mla_metadata_size_sparse(int batch, int h_q, int s_q, int h_kv, size_t *meta_bytes,
                                      size_t *num_splits_bytes);
